@@ -1,0 +1,192 @@
+/*
+ * Oracle for the paged KV attention store -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Plain, slow, single-threaded C that states what the hot path of the nano-vLLM
+ * engine computes, written from the nano-vLLM field guide (Step 05 "Blocks, block
+ * tables and slots"; Step 07.5-07.6 "prepare_prefill" / "prepare_decode"; Step 10.3
+ * "attention.py: storing K/V and calling FlashAttention").  Only tests/, the smoke
+ * check and the bench's CPU-baseline leg may load it; the product path never does.
+ * It shares no code, header or table with the CUDA library.
+ *
+ * Conventions
+ *   - bf16 values are uint16 bit patterns, widened exactly to float.
+ *   - A pool of one layer is [num_blocks, block_size, Hkv, D]; one slot is a row of
+ *     Hkv*D contiguous values, and slot = block_id * block_size + offset.
+ *   - Attention is evaluated per query and per head by its plain definition over
+ *     LOGICAL key positions j = 0..L-1:
+ *         s_j = scale * sum_d q_d k_{j,d}          (float, summed in d order)
+ *         p_j = exp(s_j - max_j s_j)               (float max-subtracted softmax)
+ *         o_d = (sum_j p_j v_{j,d}) / (sum_j p_j)  (float, summed in j order)
+ *     The output stays float, unrounded.  L == 0 gives zeros.
+ *   - GQA: q head h reads kv head h / (Hq / Hkv) (contiguous head groups; the pages
+ *     say only that several query heads share one KV head).
+ *   - Prefill with fewer queries than keys uses the bottom-right causal alignment the
+ *     field guide states for FlashAttention: query i of a chunk of Lq after P cached
+ *     tokens sees keys 0..P+i, i.e. L = P + i + 1.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -shared -fPIC (no fast-math; no FMA
+ * contraction, so x86-64 and aarch64 hosts give the same bits).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static float widen_bf16(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Field guide, "Blocks, block tables and slots": the block that holds position
+ * `pos` is table[pos / block_size]; the slot is block_id * block_size + pos % block_size. */
+int32_t oracle_slot_of(const int32_t *table, int32_t pos, int32_t block_size)
+{
+    return table[pos / block_size] * block_size + pos % block_size;
+}
+
+/* Field guide Step 10.3, the Triton store kernel: for each new-token row i, read
+ * slot_mapping[i]; -1 marks a padding row and writes nothing; otherwise copy the
+ * row's Hkv*D key values and value values into row `slot` of the flattened caches.
+ * Slots the pages never produce (below -1, or past the pool) are skipped and
+ * counted; the return value is that count. */
+int64_t oracle_store_kvcache(const uint16_t *k, int64_t k_row_stride,
+                             const uint16_t *v, int64_t v_row_stride,
+                             const int32_t *slot_mapping, int64_t n_tokens,
+                             uint16_t *k_cache, uint16_t *v_cache,
+                             int64_t num_slots, int32_t row_elems)
+{
+    int64_t rejected = 0;
+    for (int64_t i = 0; i < n_tokens; ++i) {
+        int64_t s = slot_mapping[i];
+        if (s == -1)
+            continue;
+        if (s < -1 || s >= num_slots) {
+            ++rejected;
+            continue;
+        }
+        memcpy(k_cache + s * row_elems, k + i * k_row_stride, (size_t)row_elems * sizeof(uint16_t));
+        memcpy(v_cache + s * row_elems, v + i * v_row_stride, (size_t)row_elems * sizeof(uint16_t));
+    }
+    return rejected;
+}
+
+/* One query vector against logical keys 0..L-1 of one sequence, read through its
+ * block table.  `work` holds at least L floats. */
+static void attend_one(const uint16_t *qv, int32_t L, const int32_t *table, int32_t block_size,
+                       const uint16_t *k_cache, const uint16_t *v_cache, int32_t num_kv_heads,
+                       int32_t kv_head, int32_t head_dim, float scale, float *work, float *out)
+{
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    if (L <= 0) {
+        for (int32_t t = 0; t < head_dim; ++t)
+            out[t] = 0.0f;
+        return;
+    }
+    float m = -INFINITY;
+    for (int32_t j = 0; j < L; ++j) {
+        const int64_t slot = oracle_slot_of(table, j, block_size);
+        const uint16_t *kr = k_cache + slot * row + (int64_t)kv_head * head_dim;
+        float dot = 0.0f;
+        for (int32_t t = 0; t < head_dim; ++t)
+            dot += widen_bf16(qv[t]) * widen_bf16(kr[t]);
+        const float s = scale * dot;
+        work[j] = s;
+        if (s > m)
+            m = s;
+    }
+    float sum = 0.0f;
+    for (int32_t j = 0; j < L; ++j) {
+        const float p = expf(work[j] - m);
+        work[j] = p;
+        sum += p;
+    }
+    for (int32_t t = 0; t < head_dim; ++t)
+        out[t] = 0.0f;
+    for (int32_t j = 0; j < L; ++j) {
+        const int64_t slot = oracle_slot_of(table, j, block_size);
+        const uint16_t *vr = v_cache + slot * row + (int64_t)kv_head * head_dim;
+        const float p = work[j];
+        for (int32_t t = 0; t < head_dim; ++t)
+            out[t] += p * widen_bf16(vr[t]);
+    }
+    for (int32_t t = 0; t < head_dim; ++t)
+        out[t] = out[t] / sum;
+}
+
+/* Field guide Step 10.3 (decode branch) with Step 07.6: one query per sequence at
+ * position L-1, where L = context_lens[b] already counts the token stored in the same
+ * forward; it reads keys 0..L-1 through block_tables[b].  q and out are [B, Hq, D].
+ * Sequences seq_begin..seq_end-1 are computed (the rest of `out` is untouched).
+ * Returns 0, or -1 if scratch memory could not be had. */
+int32_t oracle_decode_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                           const int32_t *block_tables, int32_t bt_stride, const int32_t *context_lens,
+                           int32_t seq_begin, int32_t seq_end, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t block_size, float scale, float *out)
+{
+    const int32_t group = num_q_heads / num_kv_heads;
+    int32_t max_len = 1;
+    for (int32_t b = seq_begin; b < seq_end; ++b)
+        if (context_lens[b] > max_len)
+            max_len = context_lens[b];
+    float *work = (float *)malloc(sizeof(float) * (size_t)max_len);
+    if (!work)
+        return -1;
+    for (int32_t b = seq_begin; b < seq_end; ++b) {
+        for (int32_t h = 0; h < num_q_heads; ++h) {
+            const int64_t r = ((int64_t)b * num_q_heads + h) * head_dim;
+            attend_one(q + r, context_lens[b], block_tables + (int64_t)b * bt_stride, block_size,
+                       k_cache, v_cache, num_kv_heads, h / group, head_dim, scale, work, out + r);
+        }
+    }
+    free(work);
+    return 0;
+}
+
+/* Field guide Step 10.3 (prefill branch, prefix cache) with Step 07.5: the new tokens
+ * of all sequences are packed; sequence b owns query rows cu_q[b]..cu_q[b+1]-1 and
+ * Lk = cu_k[b+1]-cu_k[b] keys, of which P = Lk - Lq were cached before this chunk.
+ * Query i of the chunk (absolute position P+i) sees keys 0..P+i.
+ * `rows` lists the packed query rows to compute (NULL: rows 0..n_rows-1); output row
+ * r of `out` ([n_rows, Hq, D]) is query row rows[r].  Returns 0, -1 on allocation
+ * failure, -2 if a row is outside the batch. */
+int32_t oracle_prefill_attn(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                            const int32_t *block_tables, int32_t bt_stride, int32_t num_seqs,
+                            const int64_t *rows, int64_t n_rows, int32_t num_q_heads, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t block_size, float scale, float *out)
+{
+    const int32_t group = num_q_heads / num_kv_heads;
+    int32_t max_len = 1;
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        const int32_t lk = cu_seqlens_k[b + 1] - cu_seqlens_k[b];
+        if (lk > max_len)
+            max_len = lk;
+    }
+    float *work = (float *)malloc(sizeof(float) * (size_t)max_len);
+    if (!work)
+        return -1;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const int64_t t = rows ? rows[r] : r;
+        int32_t b = 0;
+        while (b < num_seqs && !(cu_seqlens_q[b] <= t && t < cu_seqlens_q[b + 1]))
+            ++b;
+        if (b == num_seqs) {
+            free(work);
+            return -2;
+        }
+        const int32_t lq = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+        const int32_t lk = cu_seqlens_k[b + 1] - cu_seqlens_k[b];
+        const int32_t i = (int32_t)(t - cu_seqlens_q[b]);
+        const int32_t L = (lk - lq) + i + 1;
+        for (int32_t h = 0; h < num_q_heads; ++h) {
+            attend_one(q + (t * num_q_heads + h) * head_dim, L, block_tables + (int64_t)b * bt_stride,
+                       block_size, k_cache, v_cache, num_kv_heads, h / group, head_dim, scale, work,
+                       out + (r * num_q_heads + h) * head_dim);
+        }
+    }
+    free(work);
+    return 0;
+}
