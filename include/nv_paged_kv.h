@@ -1,0 +1,157 @@
+/*
+ * nv_paged_kv.h -- C ABI of the paged KV attention store for NVIDIA GB300 (sm_103a).
+ *
+ * The data-parallel hot path of a vLLM-style engine's attention layer, as the nano-vLLM
+ * field guide walks through it (Step 10.3 "attention.py: storing K/V and calling
+ * FlashAttention"): each forward first scatters the new tokens' K/V rows into a paged pool,
+ * then attends over the pool through per-sequence block tables -- one query per sequence
+ * in decode, a causal chunk after a cached prefix in prefill.
+ *
+ * Common conventions
+ *   - Every pointer is a DEVICE pointer owned by the caller.  No entry point allocates,
+ *     frees, synchronises or keeps state between calls, with two documented exceptions
+ *     that cost nothing on the device: the first call on a device reads its SM count, and
+ *     nv_paged_prefill_attn looks up the driver's tensor-map encoder once per process.
+ *     Work is enqueued on `stream` and returns at once.
+ *   - bf16 tensors are passed as `void*` (IEEE bfloat16 bit patterns).
+ *   - One layer's pool is two tensors k_cache, v_cache of shape
+ *     [num_blocks, block_size, num_kv_heads, head_dim], contiguous (the per-layer view of the
+ *     field guide's Step 07.4 KV pool).  A "slot" is one row of num_kv_heads*head_dim values;
+ *     slot = block_id * block_size + offset (Step 05.1).
+ *   - block_tables: int32 [num_seqs, bt_stride]; row b lists sequence b's physical block ids
+ *     in logical order, padded with -1 (Step 07.7).  Entries beyond the blocks a sequence's
+ *     length needs are never read.
+ *   - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *   - head_dim must be 128; block_size a power of two in [16, 256]; num_q_heads a multiple of
+ *     num_kv_heads with a group of at most 8 (decode) / 16 (prefill); num_kv_heads <= 16.
+ *   - Host-side argument errors return a negative nv_status before anything is enqueued.
+ *     Data-dependent errors found on the device (a slot or block id outside the pool, a
+ *     length beyond what the block table or the host hint allows) never fault: the offending
+ *     row or key is skipped and a bit from NV_DERR_* is OR-ed into *d_err when d_err is not
+ *     NULL (int32, caller-zeroed; read it after the stream has finished).
+ *   - The library is safe to call from several host threads; calls on different streams
+ *     may overlap on the device, except where an entry point says otherwise.
+ */
+#ifndef NV_PAGED_KV_H
+#define NV_PAGED_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle as cudaStream_t / CUstream.  NULL means the legacy default stream. */
+typedef struct CUstream_st *nv_stream_t;
+
+typedef enum nv_status {
+    NV_OK = 0,
+    NV_ERR_NULL = -1,         /* a required pointer is NULL */
+    NV_ERR_SHAPE = -2,        /* a size is negative, zero where it may not be, or inconsistent */
+    NV_ERR_ALIGN = -3,        /* a pointer or row stride breaks the 16-byte alignment rule */
+    NV_ERR_UNSUPPORTED = -4,  /* a shape outside what the kernels implement (e.g. head_dim != 128) */
+    NV_ERR_WORKSPACE = -5,    /* workspace NULL or smaller than the size query returned */
+    NV_ERR_CUDA = -6          /* the CUDA runtime reported an error (launch, attribute, driver entry) */
+} nv_status;
+
+/* Bits OR-ed into *d_err by the kernels. */
+#define NV_DERR_SLOT_RANGE 0x1    /* slot_mapping entry < -1 or >= num_slots: row skipped */
+#define NV_DERR_BLOCK_RANGE 0x2   /* a needed block-table entry outside [0, num_blocks): its keys skipped */
+#define NV_DERR_LENGTH 0x4        /* a length exceeds the block table, the host hint, or is negative */
+#define NV_DERR_TIMEOUT 0x8       /* a bounded wait on an asynchronous copy gave up */
+
+/* Human-readable name of an nv_status value (static string). */
+const char *nv_status_string(int status);
+
+/*
+ * nv_store_kvcache -- scatter new K/V rows into their cache slots.
+ *
+ * Field guide Step 10.3, "The Triton store kernel": for every new-token row i,
+ * s = slot_mapping[i]; s == -1 marks a padding row (CUDA-graph bucket padding,
+ * Step 07.8) and writes nothing; otherwise row i of k (num_kv_heads*head_dim values) goes
+ * to row s of the flattened k_cache, and likewise for v.  Bit-exact copy.
+ *
+ *   k, v          bf16 [n_tokens, num_kv_heads, head_dim]; heads contiguous (head stride
+ *                 head_dim), rows k_row_stride / v_row_stride ELEMENTS apart (v may be a view
+ *                 into a fused QKV output whose rows are wider).  Strides >= num_kv_heads*head_dim
+ *                 and multiples of 8; base pointers 16-byte aligned.
+ *   slot_mapping  int32 [n_tokens].
+ *   k_cache, v_cache  bf16 [num_slots, num_kv_heads*head_dim] (any [num_blocks, block_size, ...]
+ *                 pool flattened), 16-byte aligned.
+ *   n_tokens      >= 0 (0 enqueues nothing).
+ *   d_err         nullable; NV_DERR_SLOT_RANGE for slots outside [-1, num_slots).
+ * Duplicate slots within one call are not supported (the pages never produce them).
+ */
+int nv_store_kvcache(const void *k, int64_t k_row_stride, const void *v, int64_t v_row_stride,
+                     const int32_t *slot_mapping, int32_t n_tokens, void *k_cache, void *v_cache,
+                     int64_t num_slots, int32_t num_kv_heads, int32_t head_dim, int32_t *d_err,
+                     nv_stream_t stream);
+
+/*
+ * Bytes of workspace nv_paged_decode_attn needs for this batch (0 means none).  Depends only
+ * on its arguments, so it can be sized once for the largest batch and reused.
+ */
+size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                      int32_t max_context_len);
+
+/*
+ * nv_paged_decode_attn -- one query per sequence over its paged KV history (GQA).
+ *
+ * Field guide Step 10.3 (decode branch) and Step 07.6: sequence b has L = context_lens[b]
+ * keys -- this already counts the token whose K/V nv_store_kvcache wrote in the same forward
+ * -- read through block_tables[b]; the query sits at position L-1, so it sees every key.
+ *   out[b, h, :] = sum_j softmax_j(scale * <q[b,h,:], K_j>) * V_j,   j = 0..L-1,
+ * with K_j, V_j the kv-head (h / group) rows of slot block_tables[b][j / block_size] *
+ * block_size + j % block_size.  fp32 accumulation and softmax, bf16 output rounded once.
+ * A row with L == 0 (graph padding) gets zeros.
+ *
+ *   q, out        bf16 [num_seqs, num_q_heads, head_dim], contiguous, 16-byte aligned.
+ *   block_tables  int32 [num_seqs, bt_stride]; context_lens int32 [num_seqs].
+ *   num_blocks    pool size in blocks (block ids must lie in [0, num_blocks)).
+ *   max_context_len  host-side upper bound on every context_lens[b] (sizes the split-KV
+ *                 grid without reading device memory).  A sequence longer than it is
+ *                 truncated to it and flagged NV_DERR_LENGTH.  <= bt_stride*block_size.
+ *   scale         softmax scale (head_dim ** -0.5 in the pages).
+ *   workspace     device scratch of at least nv_paged_decode_workspace_size(...) bytes
+ *                 (may be NULL when that size is 0).  Calls that share a workspace must not
+ *                 overlap on the device.
+ */
+int nv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, int32_t bt_stride, const int32_t *context_lens,
+                         int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
+                         void *out, void *workspace, size_t workspace_bytes, int32_t *d_err,
+                         nv_stream_t stream);
+
+/*
+ * nv_paged_prefill_attn -- varlen causal prefill over a cached prefix plus the new chunk.
+ *
+ * Field guide Step 10.3 (prefill branch, prefix cache) and Step 07.5: the new tokens of all
+ * sequences are packed; sequence b owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
+ * (Lq of them) and attends to Lk = cu_seqlens_k[b+1] - cu_seqlens_k[b] keys read through
+ * block_tables[b]; P = Lk - Lq keys were cached before this chunk, and the chunk's own K/V
+ * must already be in the pool (store first).  With fewer queries than keys the causal mask
+ * is aligned bottom-right: query i of the chunk (position P+i) sees keys 0..P+i.
+ * Tensor-core (tcgen05) QK^T and PV in bf16 with fp32 accumulation; fp32 softmax; bf16 out.
+ *
+ *   q, out        bf16 [total_q, num_q_heads, head_dim], contiguous, 16-byte aligned.
+ *   cu_seqlens_q, cu_seqlens_k  int32 [num_seqs + 1], non-decreasing, starting at 0,
+ *                 with Lk >= Lq for every sequence (else NV_DERR_LENGTH; rows untouched).
+ *   max_seqlen_q  host-side upper bound on every Lq (sizes the grid).  Rows of a longer
+ *                 chunk beyond it are not computed and NV_DERR_LENGTH is set.
+ *   total_q       cu_seqlens_q[num_seqs] (rows of q and out).
+ *   k_cache, v_cache  as above; additionally num_blocks*block_size < 2^31.
+ */
+int nv_paged_prefill_attn(const void *q, const void *k_cache, const void *v_cache,
+                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                          const int32_t *block_tables, int32_t bt_stride, int32_t num_seqs,
+                          int32_t total_q, int32_t max_seqlen_q, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                          float scale, void *out, int32_t *d_err, nv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NV_PAGED_KV_H */

@@ -1,0 +1,169 @@
+"""Paged KV attention store for NVIDIA GB300 (sm_103a): Python binding of the C ABI.
+
+The three calls of the hot path, same names as the C entry points declared in
+``include/nv_paged_kv.h``:
+
+* ``nv_store_kvcache``      -- scatter new K/V rows into their cache slots;
+* ``nv_paged_decode_attn``  -- split-KV decode attention over block tables (GQA);
+* ``nv_paged_prefill_attn`` -- varlen causal prefill over a cached prefix (tcgen05).
+
+This module only marshals arguments: it reads shapes, strides and raw device pointers
+from torch tensors and the current CUDA stream, and calls the shared library through
+ctypes.  Every step of the computation runs in the library's kernels; there is no other
+implementation to fall back to, and importing fails loudly if the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import metadata  # noqa: F401  (host-side slot / cu_seqlens builders)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libnv_paged_kv.so")
+
+NV_OK = 0
+NV_DERR_SLOT_RANGE = 0x1
+NV_DERR_BLOCK_RANGE = 0x2
+NV_DERR_LENGTH = 0x4
+NV_DERR_TIMEOUT = 0x8
+
+EXPORTED = ("nv_status_string", "nv_store_kvcache", "nv_paged_decode_workspace_size", "nv_paged_decode_attn",
+            "nv_paged_prefill_attn")
+
+
+class NvError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn} returned {status}: {text}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load (once) and return the ctypes handle of the CUDA library.
+
+    Raises ``RuntimeError`` if it has not been built -- run
+    ``python -m paged_kv_attention_store_gb300.build`` (or ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built: {p} is missing "
+                           "(run `python -m paged_kv_attention_store_gb300.build`)")
+    L = ctypes.CDLL(p)
+    V, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    L.nv_status_string.argtypes = [ctypes.c_int]
+    L.nv_status_string.restype = ctypes.c_char_p
+    L.nv_store_kvcache.argtypes = [V, i64, V, i64, V, i32, V, V, i64, i32, i32, V, V]
+    L.nv_store_kvcache.restype = ctypes.c_int
+    L.nv_paged_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+    L.nv_paged_decode_workspace_size.restype = sz
+    L.nv_paged_decode_attn.argtypes = [V, V, V, V, i32, V, i32, i32, i32, i32, i32, i32, i32, f32, V, V, sz, V, V]
+    L.nv_paged_decode_attn.restype = ctypes.c_int
+    L.nv_paged_prefill_attn.argtypes = [V, V, V, V, V, V, i32, i32, i32, i32, i32, i32, i32, i32, i32, f32, V, V, V]
+    L.nv_paged_prefill_attn.restype = ctypes.c_int
+    if path is None:
+        _lib = L
+    return L
+
+
+def _check(fn, rc):
+    if rc != NV_OK:
+        raise NvError(fn, rc, load_library().nv_status_string(rc).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _pool_shape(k_cache, v_cache):
+    _need(k_cache.dim() == 4 and k_cache.shape == v_cache.shape,
+          "caches must be [num_blocks, block_size, num_kv_heads, head_dim]")
+    _need(k_cache.is_contiguous() and v_cache.is_contiguous(), "caches must be contiguous")
+    return tuple(int(x) for x in k_cache.shape)
+
+
+def nv_store_kvcache(k, v, slot_mapping, k_cache, v_cache, d_err=None, stream=None):
+    """Scatter ``k``/``v`` rows ``[N, Hkv, D]`` into ``k_cache``/``v_cache`` at ``slot_mapping`` (-1 = skip).
+
+    ``k`` and ``v`` need contiguous heads and may have any row stride (e.g. ``v`` a view
+    into a fused QKV output).  Caches are ``[num_blocks, block_size, Hkv, D]`` contiguous."""
+    nb, bs, hkv, d = _pool_shape(k_cache, v_cache)
+    n = int(slot_mapping.shape[0])
+    for name, t in (("k", k), ("v", v)):
+        _need(t.dim() == 3 and tuple(t.shape) == (n, hkv, d), f"{name} must be [N, Hkv, D] = {(n, hkv, d)}")
+        _need(t.stride(2) == 1 and t.stride(1) == d, f"{name} heads must be contiguous")
+    rc = load_library().nv_store_kvcache(_ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(slot_mapping), n,
+                                         _ptr(k_cache), _ptr(v_cache), nb * bs, hkv, d, _ptr(d_err), _stream(stream))
+    _check("nv_store_kvcache", rc)
+
+
+def nv_paged_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len) -> int:
+    return int(load_library().nv_paged_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len))
+
+
+def nv_paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, max_context_len=None,
+                         workspace=None, d_err=None, stream=None):
+    """Decode attention: ``q`` ``[B, Hq, D]`` over each sequence's ``context_lens[b]`` keys.
+
+    ``max_context_len`` (a host int bounding every context length) sizes the split-KV grid;
+    by default it is the block table's capacity ``W * block_size``, which needs no device
+    read.  ``workspace`` is allocated with torch when not given."""
+    import torch
+    nb, bs, hkv, d = _pool_shape(k_cache, v_cache)
+    B, hq, dq = (int(x) for x in q.shape)
+    _need(dq == d and q.is_contiguous(), "q must be contiguous [B, Hq, D]")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == B and block_tables.stride(1) == 1,
+          "block_tables must be [B, W] with unit column stride")
+    if max_context_len is None:
+        max_context_len = int(block_tables.shape[1]) * bs
+    if out is None:
+        out = torch.empty_like(q)
+    ws_need = nv_paged_decode_workspace_size(B, hq, d, int(max_context_len))
+    if workspace is None and ws_need:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().nv_paged_decode_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.stride(0), _ptr(context_lens), B, hq,
+        hkv, d, bs, nb, int(max_context_len), float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_err),
+        _stream(stream))
+    _check("nv_paged_decode_attn", rc)
+    return out
+
+
+def nv_paged_prefill_attn(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables, scale, max_seqlen_q=None,
+                          out=None, d_err=None, stream=None):
+    """Causal varlen prefill: packed ``q`` ``[total_q, Hq, D]`` over cached prefix + chunk.
+
+    ``max_seqlen_q`` (host int) sizes the grid; by default ``total_q``, an upper bound that
+    needs no device read (surplus CTAs exit at once)."""
+    import torch
+    nb, bs, hkv, d = _pool_shape(k_cache, v_cache)
+    total_q, hq, dq = (int(x) for x in q.shape)
+    _need(dq == d and q.is_contiguous(), "q must be contiguous [total_q, Hq, D]")
+    B = int(cu_seqlens_q.shape[0]) - 1
+    _need(int(cu_seqlens_k.shape[0]) == B + 1, "cu_seqlens_q and cu_seqlens_k must both have B+1 entries")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == B and block_tables.stride(1) == 1,
+          "block_tables must be [B, W] with unit column stride")
+    if out is None:
+        out = torch.empty_like(q)
+    rc = load_library().nv_paged_prefill_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(block_tables),
+        block_tables.stride(0), B, total_q, int(total_q if max_seqlen_q is None else max_seqlen_q), hq, hkv, d, bs,
+        nb, float(scale), _ptr(out), _ptr(d_err), _stream(stream))
+    _check("nv_paged_prefill_attn", rc)
+    return out

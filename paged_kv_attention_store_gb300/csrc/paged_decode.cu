@@ -1,0 +1,512 @@
+// nv_paged_decode_attn: split-KV flash-decoding over a paged KV pool (GQA), CUDA cores.
+//
+// What it computes is the decode branch of the nano-vLLM field guide's Step 10.3: for
+// sequence b with L = context_lens[b] keys (the token stored in this same forward included,
+// Step 07.6) and query head h, out[b,h] = softmax_j(scale * q[b,h] . K_j) V_j over the
+// kv-head h/group rows of the L logical positions, read through block_tables[b].
+//
+// How (GB300 design; the pages call a library kernel here):
+//   * Work unit = (sequence, split of `split_tokens` consecutive positions).  One CTA takes
+//     ALL kv heads of its unit, so each position's K (and V) row of Hkv*128 bf16 values is
+//     one contiguous run in the pool, and T consecutive positions inside a block are one
+//     contiguous run of T*Hkv*256 bytes: a single 1-D TMA bulk copy moves them into shared
+//     memory, completing on an mbarrier.  A producer warp keeps kStages such chunks in
+//     flight per CTA (two CTAs per SM), reading one block-table entry per block.
+//   * Consumer warp w owns kv head w and its G = Hq/Hkv query heads, so every K/V element
+//     is read from shared memory once and used G times (GQA sharing).  A half-warp handles
+//     one position at a time, each lane 8 of the 128 dims; partial dot products are reduced
+//     with a reduce-scatter over 4 shuffle levels that leaves each lane the full score of
+//     one of the G heads, so the exponential is computed once per (position, head).
+//   * Online softmax in base 2 with a lazy rescale: the running max only moves when a score
+//     exceeds it by more than 8 (a factor 256), which keeps the rescale branch rare; the
+//     weights then stay below 2^8 and the accumulation in fp32 is unaffected.
+//   * HBM-bound (about 4 flop per byte of KV), so no tensor cores: fp32 FMAs on CUDA cores.
+//   * A sequence split over several CTAs writes unnormalised partial outputs plus its
+//     (max, sum); a small merge kernel combines them.  Single-split sequences write bf16
+//     output directly.
+#include "nv_common.cuh"
+
+namespace {
+
+using namespace nvkv;
+
+constexpr int kD = 128;           // head_dim
+constexpr int kT = 8;             // positions per staged chunk
+constexpr int kStages = 3;        // chunks in flight per CTA
+constexpr float kRescaleLog2 = 8.0f;
+
+struct DecodeParams {
+    const __nv_bfloat16 *q;
+    const __nv_bfloat16 *k_cache;
+    const __nv_bfloat16 *v_cache;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    __nv_bfloat16 *out;
+    float *part_o;      // [num_seqs, max_splits, Hq, 128]
+    float *part_ml;     // [num_seqs, max_splits, Hq, 2]
+    int32_t *d_err;
+    int32_t bt_stride;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t block_shift;
+    int32_t num_blocks;
+    int32_t max_len;    // min(max_context_len, bt_stride * block_size)
+    int32_t split_tokens;
+    int32_t max_splits;
+    float scale_log2;   // scale * log2(e)
+};
+
+// Reduce G per-lane partial sums over the 16 lanes of a half-warp so that each lane ends
+// with the FULL sum of exactly one of the G values: lane sl holds value sl / (16 / G).
+template <int G>
+__device__ __forceinline__ float reduce_to_owner(const float (&x)[G], int sl)
+{
+    float v[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i)
+        v[i] = x[i];
+    int cnt = G;
+#pragma unroll
+    for (int mask = 8; mask >= 1; mask >>= 1) {
+        if (cnt > 1) {
+            const bool hi = (sl & mask) != 0;
+#pragma unroll
+            for (int i = 0; i < G / 2; ++i) {
+                if (i < cnt / 2) {
+                    const float keep = hi ? v[cnt / 2 + i] : v[i];
+                    const float send = hi ? v[i] : v[cnt / 2 + i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+                }
+            }
+            cnt /= 2;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
+        }
+    }
+    return v[0];
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &r, float (&f)[8])
+{
+    f[0] = bf16lo(r.x);
+    f[1] = bf16hi(r.x);
+    f[2] = bf16lo(r.y);
+    f[3] = bf16hi(r.y);
+    f[4] = bf16lo(r.z);
+    f[5] = bf16hi(r.z);
+    f[6] = bf16lo(r.w);
+    f[7] = bf16hi(r.w);
+}
+
+template <int G, int MAX_KV_HEADS>
+__global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 2 : 1))
+    paged_decode_kernel(const DecodeParams p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int hkv = p.num_kv_heads;
+    const int dkv = hkv * kD;                        // elements per pool row
+    const uint32_t chunk_bytes = (uint32_t)kT * dkv * 2;  // one K (or V) chunk
+    const int b = blockIdx.x;
+    const int split = blockIdx.y;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    int L = __ldg(p.context_lens + b);
+    if (L < 0 || L > p.max_len) {
+        if (split == 0 && threadIdx.x == 0)
+            flag_error(p.d_err, NV_DERR_LENGTH);
+        L = L < 0 ? 0 : p.max_len;
+    }
+    const int t0 = split * p.split_tokens;
+    if (L == 0) {
+        if (split == 0) {   // padding row: attends to nothing, writes zeros
+            uint4 *o = reinterpret_cast<uint4 *>(p.out + (size_t)b * p.num_q_heads * kD);
+            for (int i = threadIdx.x; i < p.num_q_heads * kD / 8; i += blockDim.x)
+                o[i] = make_uint4(0, 0, 0, 0);
+        }
+        return;
+    }
+    if (t0 >= L)
+        return;
+    const int t1 = min(L, t0 + p.split_tokens);
+    const int nsplit = (L + p.split_tokens - 1) / p.split_tokens;
+    const int nchunks = (t1 - t0 + kT - 1) / kT;
+
+    // shared memory: [kStages][K chunk | V chunk], then barriers and per-stage valid counts
+    const uint32_t stage_bytes = 2 * chunk_bytes;
+    uint8_t *tail = smem + (size_t)kStages * stage_bytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tail);   // full[kStages], empty[kStages]
+    int32_t *valid_rows = reinterpret_cast<int32_t *>(tail + 2 * kStages * sizeof(uint64_t));
+    const uint32_t smem_base = smem_u32(smem);
+    const uint32_t bar_base = smem_u32(bars);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar_base + 8 * s, 1);                    // full: producer arrive + tx bytes
+            mbar_init(bar_base + 8 * (kStages + s), hkv);      // empty: one arrive per consumer warp
+        }
+        fence_barrier_init();
+    }
+    // Rows a partial chunk does not copy keep stale-but-finite values (zero at first).
+    for (uint32_t i = threadIdx.x; i < (uint32_t)kStages * stage_bytes / 16; i += blockDim.x)
+        sts_u4(smem_base + 16 * i, make_uint4(0, 0, 0, 0));
+    fence_proxy_async_smem();   // the zeros must land before any bulk copy writes these bytes
+    __syncthreads();
+
+    if (warp == hkv) {
+        // ---------------- producer: one lane issues the bulk copies ----------------
+        if (lane == 0) {
+            const int bs_mask = (1 << p.block_shift) - 1;
+            const int32_t *bt = p.block_tables + (size_t)b * p.bt_stride;
+            int cur_lblk = -1;
+            int64_t blk_slot0 = 0;
+            bool blk_ok = false;
+            int issued = 0;
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c % kStages;
+                if (c >= kStages && !mbar_wait(bar_base + 8 * (kStages + s), ((c / kStages) - 1) & 1)) {
+                    flag_error(p.d_err, NV_DERR_TIMEOUT);
+                    break;
+                }
+                const int tok0 = t0 + c * kT;
+                const int n = min(kT, t1 - tok0);
+                const int lblk = tok0 >> p.block_shift;
+                if (lblk != cur_lblk) {
+                    cur_lblk = lblk;
+                    const int blk = __ldg(bt + lblk);
+                    blk_ok = blk >= 0 && blk < p.num_blocks;
+                    if (!blk_ok)
+                        flag_error(p.d_err, NV_DERR_BLOCK_RANGE);
+                    blk_slot0 = (int64_t)blk << p.block_shift;
+                }
+                const uint32_t full = bar_base + 8 * s;
+                if (blk_ok) {
+                    valid_rows[s] = n;
+                    const int64_t slot = blk_slot0 + (tok0 & bs_mask);
+                    const uint32_t bytes = (uint32_t)n * dkv * 2;
+                    mbar_arrive_expect_tx(full, 2 * bytes);
+                    bulk_g2s(smem_base + s * stage_bytes, p.k_cache + slot * dkv, bytes, full);
+                    bulk_g2s(smem_base + s * stage_bytes + chunk_bytes, p.v_cache + slot * dkv, bytes, full);
+                } else {
+                    valid_rows[s] = 0;     // keys of an out-of-pool block are treated as absent
+                    mbar_arrive(full);
+                }
+                issued = c + 1;
+            }
+            // Do not leave while copies still land in this CTA's shared memory.
+            for (int c = max(0, issued - kStages); c < issued; ++c)
+                mbar_wait(bar_base + 8 * (c % kStages), (c / kStages) & 1);
+        }
+        return;
+    }
+
+    // ---------------- consumers: warp w = kv head w, its G query heads ----------------
+    const int kvh = warp;
+    const int half = lane >> 4;
+    const int sl = lane & 15;
+    constexpr int kLanesPerHead = 16 / G;
+    const int head0 = kvh * G;
+
+    float qf[G][8];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const uint4 r = *reinterpret_cast<const uint4 *>(p.q + ((size_t)b * p.num_q_heads + head0 + g) * kD + sl * 8);
+        unpack8(r, qf[g]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            qf[g][i] *= p.scale_log2;
+    }
+    float acc[G][8];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            acc[g][i] = 0.f;
+    float m_run = -INFINITY;   // running max (log2 units) of head own_g, this half's positions
+    float l_run = 0.f;         // running sum of weights of head own_g
+
+    // lane's column inside a staged row: kv head kvh, dims sl*8 .. sl*8+7
+    const uint32_t col_off = (uint32_t)(kvh * kD + sl * 8) * 2;
+    const uint32_t row_bytes = (uint32_t)dkv * 2;
+    bool ok = true;
+    for (int c = 0; c < nchunks && ok; ++c) {
+        const int s = c % kStages;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_base + 8 * s, (c / kStages) & 1))) {
+            if (lane == 0)
+                flag_error(p.d_err, NV_DERR_TIMEOUT);
+            ok = false;
+            break;
+        }
+        const int nvalid = valid_rows[s];
+        const uint32_t kbase = smem_base + s * stage_bytes + col_off;
+        const uint32_t vbase = kbase + chunk_bytes;
+
+        float sc[kT / 2];
+#pragma unroll
+        for (int jj = 0; jj < kT / 2; ++jj) {
+            const int j = half * (kT / 2) + jj;
+            float kf[8];
+            unpack8(lds_u4(kbase + j * row_bytes), kf);
+            float part[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float a = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    a = fmaf(qf[g][i], kf[i], a);
+                part[g] = a;
+            }
+            const float full = reduce_to_owner<G>(part, sl);
+            sc[jj] = (j < nvalid) ? full : -INFINITY;
+        }
+        float mx = sc[0];
+#pragma unroll
+        for (int jj = 1; jj < kT / 2; ++jj)
+            mx = fmaxf(mx, sc[jj]);
+        const bool need = mx > m_run + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? fast_exp2(m_run - mx) : 1.f;   // m_run = -inf -> 0
+            if (need)
+                m_run = mx;
+            l_run *= alpha;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float a = __shfl_sync(0xffffffffu, alpha, (half << 4) + g * kLanesPerHead);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    acc[g][i] *= a;
+            }
+        }
+        float pj[kT / 2];
+#pragma unroll
+        for (int jj = 0; jj < kT / 2; ++jj) {
+            pj[jj] = (sc[jj] == -INFINITY) ? 0.f : fast_exp2(sc[jj] - m_run);
+            l_run += pj[jj];
+        }
+#pragma unroll
+        for (int jj = 0; jj < kT / 2; ++jj) {
+            const int j = half * (kT / 2) + jj;
+            float vf[8];
+            unpack8(lds_u4(vbase + j * row_bytes), vf);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float pg = __shfl_sync(0xffffffffu, pj[jj], (half << 4) + g * kLanesPerHead);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    acc[g][i] = fmaf(pg, vf[i], acc[g][i]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(bar_base + 8 * (kStages + s));
+    }
+
+    // ---- merge the two half-warps (they saw disjoint positions), then write ----
+    float m_g[G], l_g[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        m_g[g] = __shfl_sync(0xffffffffu, m_run, (half << 4) + g * kLanesPerHead);
+        l_g[g] = __shfl_sync(0xffffffffu, l_run, (half << 4) + g * kLanesPerHead);
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m_g[g], 16);
+        const float lo = __shfl_xor_sync(0xffffffffu, l_g[g], 16);
+        const float M = fmaxf(m_g[g], mo);
+        const float fa = (m_g[g] == -INFINITY) ? 0.f : fast_exp2(m_g[g] - M);
+        const float fb = (mo == -INFINITY) ? 0.f : fast_exp2(mo - M);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float other = __shfl_xor_sync(0xffffffffu, acc[g][i], 16);
+            acc[g][i] = acc[g][i] * fa + other * fb;
+        }
+        m_g[g] = M;
+        l_g[g] = l_g[g] * fa + lo * fb;
+    }
+
+    if (nsplit == 1) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            if ((G == 1 && half == 0) || (G > 1 && (g & 1) == half)) {
+                const float inv = l_g[g] > 0.f ? 1.f / l_g[g] : 0.f;
+                uint4 w;
+                w.x = pack_bf16x2(acc[g][0] * inv, acc[g][1] * inv);
+                w.y = pack_bf16x2(acc[g][2] * inv, acc[g][3] * inv);
+                w.z = pack_bf16x2(acc[g][4] * inv, acc[g][5] * inv);
+                w.w = pack_bf16x2(acc[g][6] * inv, acc[g][7] * inv);
+                *reinterpret_cast<uint4 *>(p.out + ((size_t)b * p.num_q_heads + head0 + g) * kD + sl * 8) = w;
+            }
+        }
+    } else {
+        const size_t unit = (size_t)b * p.max_splits + split;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            if ((G == 1 && half == 0) || (G > 1 && (g & 1) == half)) {
+                float *po = p.part_o + (unit * p.num_q_heads + head0 + g) * kD + sl * 8;
+                *reinterpret_cast<float4 *>(po) = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+                *reinterpret_cast<float4 *>(po + 4) = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
+                if (sl == 0)
+                    *reinterpret_cast<float2 *>(p.part_ml + (unit * p.num_q_heads + head0 + g) * 2) =
+                        make_float2(m_g[g], l_g[g]);
+            }
+        }
+    }
+}
+
+// Combine the partial results of sequences that were split: o = sum_s 2^(m_s-M) o_s /
+// sum_s 2^(m_s-M) l_s.  One CTA per sequence; a thread owns 4 dims of one head.
+__global__ void __launch_bounds__(256) merge_splits_kernel(const DecodeParams p)
+{
+    const int b = blockIdx.x;
+    int L = __ldg(p.context_lens + b);
+    L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
+    const int nsplit = (L + p.split_tokens - 1) / p.split_tokens;
+    if (nsplit <= 1)
+        return;
+    const int items = p.num_q_heads * (kD / 4);
+    for (int it = threadIdx.x; it < items; it += blockDim.x) {
+        const int h = it / (kD / 4);
+        const int d4 = it % (kD / 4);
+        float M = -INFINITY;
+        for (int s = 0; s < nsplit; ++s)
+            M = fmaxf(M, p.part_ml[(((size_t)b * p.max_splits + s) * p.num_q_heads + h) * 2]);
+        float den = 0.f, n0 = 0.f, n1 = 0.f, n2 = 0.f, n3 = 0.f;
+        for (int s = 0; s < nsplit; ++s) {
+            const size_t unit = (size_t)b * p.max_splits + s;
+            const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + (unit * p.num_q_heads + h) * 2);
+            const float w = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
+            const float4 o = *reinterpret_cast<const float4 *>(p.part_o + (unit * p.num_q_heads + h) * kD + d4 * 4);
+            den = fmaf(w, ml.y, den);
+            n0 = fmaf(w, o.x, n0);
+            n1 = fmaf(w, o.y, n1);
+            n2 = fmaf(w, o.z, n2);
+            n3 = fmaf(w, o.w, n3);
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        uint2 w2;
+        w2.x = pack_bf16x2(n0 * inv, n1 * inv);
+        w2.y = pack_bf16x2(n2 * inv, n3 * inv);
+        *reinterpret_cast<uint2 *>(p.out + ((size_t)b * p.num_q_heads + h) * kD + d4 * 4) = w2;
+    }
+}
+
+// Positions per split: aim for at least ~1200 work units so every SM has several, but keep
+// units long enough (>= 64 positions) that the partial-output traffic stays a few percent.
+int decode_split_tokens(int num_seqs, int max_context_len)
+{
+    int split = 512;
+    while (split > 64 && (int64_t)num_seqs * ((max_context_len + split - 1) / split) < 1200)
+        split >>= 1;
+    return split;
+}
+
+template <int G, int MAXH>
+int launch_decode(const DecodeParams &p, int num_seqs, size_t smem_bytes, cudaStream_t stream)
+{
+    static bool configured = false;   // benign race: every thread sets the same attribute value
+    if (!configured) {
+        if (cudaFuncSetAttribute(paged_decode_kernel<G, MAXH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_bytes > 200 * 1024 ? 227 * 1024 : 200 * 1024) != cudaSuccess)
+            return NV_ERR_CUDA;
+        configured = true;
+    }
+    dim3 grid(num_seqs, p.max_splits);
+    paged_decode_kernel<G, MAXH><<<grid, (p.num_kv_heads + 1) * 32, smem_bytes, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess)
+        return NV_ERR_CUDA;
+    if (p.max_splits > 1) {
+        merge_splits_kernel<<<num_seqs, 256, 0, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess)
+            return NV_ERR_CUDA;
+    }
+    return NV_OK;
+}
+
+template <int MAXH>
+int dispatch_group(int group, const DecodeParams &p, int num_seqs, size_t smem, cudaStream_t st)
+{
+    switch (group) {
+    case 1: return launch_decode<1, MAXH>(p, num_seqs, smem, st);
+    case 2: return launch_decode<2, MAXH>(p, num_seqs, smem, st);
+    case 4: return launch_decode<4, MAXH>(p, num_seqs, smem, st);
+    case 8: return launch_decode<8, MAXH>(p, num_seqs, smem, st);
+    default: return NV_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+extern "C" size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
+                                                 int32_t max_context_len)
+{
+    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim != kD || max_context_len <= 0)
+        return 0;
+    const int split = decode_split_tokens(num_seqs, max_context_len);
+    const int max_splits = (max_context_len + split - 1) / split;
+    if (max_splits <= 1)
+        return 0;
+    return (size_t)num_seqs * max_splits * num_q_heads * (kD + 2) * sizeof(float);
+}
+
+extern "C" int nv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *block_tables, int32_t bt_stride, const int32_t *context_lens,
+                                    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
+                                    void *out, void *workspace, size_t workspace_bytes, int32_t *d_err,
+                                    nv_stream_t stream)
+{
+    using namespace nvkv_host;
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || bt_stride <= 0 || num_blocks < 0 ||
+        max_context_len < 0)
+        return NV_ERR_SHAPE;
+    if (num_seqs == 0)
+        return NV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return NV_ERR_NULL;
+    if (head_dim != kD)
+        return NV_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads != 0)
+        return NV_ERR_SHAPE;
+    const int group = num_q_heads / num_kv_heads;
+    if (num_kv_heads > 16 || (group != 1 && group != 2 && group != 4 && group != 8))
+        return NV_ERR_UNSUPPORTED;
+    if (!is_pow2(block_size) || block_size < 16 || block_size > 256)
+        return NV_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return NV_ERR_ALIGN;
+    if ((int64_t)num_blocks * block_size * num_kv_heads * kD >= (1ll << 40))
+        return NV_ERR_UNSUPPORTED;
+    if (max_context_len == 0)
+        max_context_len = 1;   // every row is padding; one split writes the zeros
+    const int64_t bt_cap = (int64_t)bt_stride * block_size;
+    const int max_len = (int)(bt_cap < max_context_len ? bt_cap : max_context_len);
+
+    DecodeParams p{};
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k_cache = static_cast<const __nv_bfloat16 *>(k_cache);
+    p.v_cache = static_cast<const __nv_bfloat16 *>(v_cache);
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.d_err = d_err;
+    p.bt_stride = bt_stride;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.block_shift = ilog2(block_size);
+    p.num_blocks = num_blocks;
+    p.max_len = max_len;
+    p.split_tokens = decode_split_tokens(num_seqs, max_context_len);
+    p.max_splits = (max_len + p.split_tokens - 1) / p.split_tokens;
+    p.scale_log2 = scale * nvkv::kLog2e;
+    if (p.max_splits > 1) {
+        const size_t need = nv_paged_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len);
+        if (!workspace || workspace_bytes < need || !aligned16(workspace))
+            return NV_ERR_WORKSPACE;
+        p.part_o = static_cast<float *>(workspace);
+        p.part_ml = p.part_o + (size_t)num_seqs * p.max_splits * num_q_heads * kD;
+    }
+    const size_t smem = (size_t)kStages * 2 * kT * num_kv_heads * kD * 2 + 2 * kStages * 8 + kStages * 4 + 16;
+    if (num_kv_heads <= 8)
+        return dispatch_group<8>(group, p, num_seqs, smem, (cudaStream_t)stream);
+    return dispatch_group<16>(group, p, num_seqs, smem, (cudaStream_t)stream);
+}

@@ -1,0 +1,115 @@
+"""The C ABI on the host, no GPU: the library builds, loads, exports every declared entry
+point, and rejects bad arguments with the documented status before touching the device."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+import paged_kv_attention_store_gb300 as nv
+from paged_kv_attention_store_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+NV_ERR_NULL, NV_ERR_SHAPE, NV_ERR_ALIGN, NV_ERR_UNSUPPORTED, NV_ERR_WORKSPACE, NV_ERR_CUDA = -1, -2, -3, -4, -5, -6
+FAKE = 0x10000          # a 16-byte-aligned address that is never dereferenced (validation fails first)
+MISALIGNED = 0x10008
+
+
+def declared_entry_points():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w \*]*?\b(nv_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("no CUDA toolkit to build the library")
+    B.build()
+    return nv.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_entry_points()
+    assert {"nv_store_kvcache", "nv_paged_decode_attn", "nv_paged_prefill_attn"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(nv.EXPORTED) <= set(names)
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert lib.nv_status_string(code)
+    assert b"unknown" in lib.nv_status_string(42)
+
+
+def _store(lib, k=FAKE, v=FAKE, sm=FAKE, n=4, kc=FAKE, vc=FAKE, ks=1024, vs=1024, hkv=8, d=128, slots=1024):
+    return lib.nv_store_kvcache(k, ks, v, vs, sm, n, kc, vc, slots, hkv, d, None, None)
+
+
+def test_store_validation(lib):
+    assert _store(lib, n=0, k=None) == 0                  # nothing to do, nothing read
+    assert _store(lib, n=-1) == NV_ERR_SHAPE
+    assert _store(lib, k=None) == NV_ERR_NULL
+    assert _store(lib, sm=None) == NV_ERR_NULL
+    assert _store(lib, ks=512) == NV_ERR_SHAPE            # row stride below Hkv*D
+    assert _store(lib, vs=1028) == NV_ERR_ALIGN           # not a multiple of 8 elements
+    assert _store(lib, k=MISALIGNED) == NV_ERR_ALIGN
+    assert _store(lib, kc=MISALIGNED) == NV_ERR_ALIGN
+    assert _store(lib, hkv=1, d=4, ks=8, vs=8) == NV_ERR_UNSUPPORTED   # row of 4 values
+
+
+def _decode(lib, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, bts=16, cl=FAKE, B=4, hq=32, hkv=8, d=128, bs=256, nb=64,
+            maxc=4096, out=FAKE, ws=None, wsb=0):
+    return lib.nv_paged_decode_attn(q, kc, vc, bt, bts, cl, B, hq, hkv, d, bs, nb, maxc, 0.088, out, ws, wsb,
+                                    None, None)
+
+
+def test_decode_validation(lib):
+    assert _decode(lib, B=0, q=None) == 0
+    assert _decode(lib, q=None) == NV_ERR_NULL
+    assert _decode(lib, cl=None) == NV_ERR_NULL
+    assert _decode(lib, d=64) == NV_ERR_UNSUPPORTED
+    assert _decode(lib, hq=12) == NV_ERR_SHAPE            # not a multiple of Hkv
+    assert _decode(lib, hq=24, hkv=8) == NV_ERR_UNSUPPORTED   # group 3
+    assert _decode(lib, bs=8) == NV_ERR_UNSUPPORTED
+    assert _decode(lib, bs=48) == NV_ERR_UNSUPPORTED
+    assert _decode(lib, out=MISALIGNED) == NV_ERR_ALIGN
+    need = lib.nv_paged_decode_workspace_size(4, 32, 128, 4096)
+    assert need > 0
+    assert _decode(lib) == NV_ERR_WORKSPACE
+    assert _decode(lib, ws=FAKE, wsb=need - 16) == NV_ERR_WORKSPACE
+    assert lib.nv_paged_decode_workspace_size(4, 32, 128, 64) == 0   # one split: no workspace
+
+
+def _prefill(lib, q=FAKE, kc=FAKE, vc=FAKE, cq=FAKE, ck=FAKE, bt=FAKE, bts=8, B=2, tq=100, mq=80, hq=16, hkv=8,
+             d=128, bs=256, nb=16, out=FAKE):
+    return lib.nv_paged_prefill_attn(q, kc, vc, cq, ck, bt, bts, B, tq, mq, hq, hkv, d, bs, nb, 0.088, out, None,
+                                     None)
+
+
+def test_prefill_validation(lib):
+    assert _prefill(lib, tq=0, q=None) == 0
+    assert _prefill(lib, cq=None) == NV_ERR_NULL
+    assert _prefill(lib, d=256) == NV_ERR_UNSUPPORTED
+    assert _prefill(lib, hq=24) == NV_ERR_UNSUPPORTED      # group 3
+    assert _prefill(lib, hq=20) == NV_ERR_SHAPE
+    assert _prefill(lib, bs=512) == NV_ERR_UNSUPPORTED
+    assert _prefill(lib, kc=MISALIGNED) == NV_ERR_ALIGN
+    assert _prefill(lib, nb=0) == NV_ERR_SHAPE
+
+
+@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="checks the no-GPU path only")
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    """With no GPU the runtime cannot launch: the entry point says so instead of crashing."""
+    assert _store(lib) == NV_ERR_CUDA
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        nv.load_library(str(tmp_path / "missing.so"))

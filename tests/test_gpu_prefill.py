@@ -1,0 +1,106 @@
+"""nv_paged_prefill_attn on the GPU against the oracle (store the chunk first, then prefill)."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from tests.gpu_util import DeviceBatch, compare, host_bits, host_f32, oracle_cache_after_store, oracle_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(batch, max_seqlen_q=None):
+    db = DeviceBatch(batch)
+    db.store()
+    out = db.prefill(max_seqlen_q)
+    assert db.err() == 0
+    kc1, vc1 = oracle_cache_after_store(oracle.default(), batch, db.kc_host0, db.vc_host0)
+    return db, host_f32(out), kc1, vc1
+
+
+CASES = [
+    # name, prefix lens, chunk lens, Hq, Hkv, block_size
+    ("g2-bs256-fresh", [0, 0], [1, 300], 16, 8, 256),
+    ("g2-bs256-prefix", [256, 512, 0, 1024], [64, 65, 128, 200], 16, 8, 256),
+    ("g2-bs16-ragged", [0, 48, 16, 160], [63, 1, 129, 77], 16, 8, 16),
+    ("g1-bs64", [64, 0, 320], [130, 5, 300], 8, 8, 64),
+    ("g4-bs128", [128, 0, 256], [33, 97, 250], 32, 8, 128),
+    ("g8-bs32", [32, 0], [40, 17], 16, 2, 32),
+    ("g16-bs256", [256], [20], 16, 1, 256),
+    ("unaligned-prefix", [100, 37, 255], [60, 200, 3], 16, 8, 16),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_prefill_shapes(case):
+    name, P, Lq, hq, hkv, bs = case
+    b = W.make_prefill(name, 31, P, Lq, hq, hkv, 128, bs, poison_tail=True)
+    db, got, kc, vc = _run(b)
+    want = oracle_prefill(oracle.default(), b, kc, vc)
+    compare(got, want, name)
+
+
+def test_prefill_single_key_is_exact():
+    b = W.make_prefill("one", 32, [0], [1], 16, 8, 128, 256, poison_tail=True)
+    db = DeviceBatch(b)
+    db.store()
+    bits = host_bits(db.prefill())
+    g = 2
+    for h in range(16):
+        assert np.array_equal(bits[0, h], b.v_new[0, h // g])
+
+
+def test_prefill_chunked_equals_full():
+    """One sequence prefilled whole, and as a cached prefix + chunk over the same pool."""
+    import torch
+    import paged_kv_attention_store_gb300 as nv
+    from tests.gpu_util import dev_i32
+    full = W.make_prefill("full", 33, [0], [700], 16, 8, 128, 64)
+    db = DeviceBatch(full)
+    db.store()
+    out_full = host_f32(db.prefill())
+    P = 384
+    out_chunk = nv.nv_paged_prefill_attn(db.q[P:].contiguous(), db.k_cache, db.v_cache, dev_i32(np.array([0, 700 - P])),
+                                         dev_i32(np.array([0, 700])), db.block_tables, full.scale)
+    compare(host_f32(out_chunk), out_full[P:], "chunk vs full")
+
+
+def test_prefill_last_row_equals_decode():
+    b = W.make_prefill("lastrow", 34, [128, 0], [77, 200], 16, 8, 128, 64)
+    db = DeviceBatch(b)
+    db.store()
+    out = host_f32(db.prefill())
+    import paged_kv_attention_store_gb300 as nv
+    from tests.gpu_util import dev_i32
+    last = b.cu_seqlens_q[1:] - 1
+    q_last = db.q[last.tolist()].contiguous()
+    dec = nv.nv_paged_decode_attn(q_last, db.k_cache, db.v_cache, db.block_tables, db.seq_lens, b.scale)
+    compare(host_f32(dec), out[last], "decode vs last prefill row")
+
+
+def test_prefill_chunk_budget_full_size_sampled():
+    """The chunked-prefill workload at full size (16 sequences, 16384 new tokens, prefixes up to
+    2048): rows sampled at the start, end and tile edges of every sequence plus a random draw."""
+    b = W.prefill_chunk()
+    db, got, kc, vc = _run(b)
+    cu = b.cu_seqlens_q
+    rows = set()
+    rng = np.random.default_rng(1)
+    for s in range(b.num_seqs):
+        lo, hi = int(cu[s]), int(cu[s + 1])
+        for r in (lo, lo + 1, lo + 63, lo + 64, hi - 65, hi - 2, hi - 1):
+            if lo <= r < hi:
+                rows.add(r)
+    rows |= set(rng.choice(int(cu[-1]), 96, replace=False).tolist())
+    rows = np.array(sorted(rows), np.int64)
+    want = oracle_prefill(oracle.default(), b, kc, vc, rows=rows, threads=16)
+    compare(got[rows], want, "prefill chunk budget")
+
+
+def test_prefill_grid_hint_smaller_than_chunk_is_flagged():
+    import paged_kv_attention_store_gb300 as nv
+    b = W.make_prefill("hint", 35, [0], [300], 16, 8, 128, 256)
+    db = DeviceBatch(b)
+    db.store()
+    db.prefill(max_seqlen_q=100)
+    assert db.err() & nv.NV_DERR_LENGTH
