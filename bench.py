@@ -1,0 +1,530 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV attention store on GB300.
+
+One JSON line on rank 0.  Two phases run in one invocation and together cover every step
+of the hot path (slot scatter, paged decode attention, varlen prefill attention):
+
+* decode phase (the headline line): K engine decode steps on the Qwen3-8B-shaped batch
+  (512 sequences, context lengths U[1024, 4096], 32 q / 8 kv heads, head_dim 128, block
+  size 256): store the 512 new K/V rows, then decode.  ``value`` is the KV bytes the
+  decode attention must read per step (4096 B per attended position: K and V of 8 heads
+  x 128 dims in bf16) times K, over the device time of the K steps: paged-decode KV GB/s.
+* prefill phase (the ``prefill`` object): K engine prefill steps on the chunked-prefill
+  workload (16 sequences, 16384 new tokens, cached prefixes 256*U{0..8}, 16 q / 8 kv
+  heads): store the 16384 new rows, then causal prefill.  TFLOP/s counts the causally
+  visible (query, key) pairs only: 4 * D * Hq per pair.
+
+``--impl reference`` times the CPU oracle (the only reference implementation this project
+has) on bounded samples of the same workloads.  Multi-GPU runs (torchrun) give every rank
+its own batch (weak scaling; the path needs no collective): barrier + synchronize around
+the timed region, max time over ranks, whole-job throughput on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged-decode KV GB/s (% of HBM peak); prefill attn TFLOP/s; attended tok/s"
+KV_BYTES_PER_TOKEN_PER_KVHEAD = 128 * 2 * 2          # K and V rows of one kv head, bf16
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------------------
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def decode_algorithmic_bytes(b: W.PagedBatch) -> int:
+    """KV rows read + q read + out written + block-table entries and lengths read."""
+    kv = int(b.seq_lens.astype(np.int64).sum()) * b.num_kv_heads * KV_BYTES_PER_TOKEN_PER_KVHEAD
+    qo = 2 * b.num_seqs * b.num_q_heads * 128 * 2
+    meta = sum(W.blocks_needed(int(L), b.block_size) for L in b.seq_lens) * 4 + b.num_seqs * 4
+    return kv + qo + meta
+
+
+def decode_kv_bytes(b: W.PagedBatch) -> int:
+    return int(b.seq_lens.astype(np.int64).sum()) * b.num_kv_heads * KV_BYTES_PER_TOKEN_PER_KVHEAD
+
+
+def prefill_pairs(b: W.PagedBatch) -> int:
+    P = b.meta["prefix_lens"].astype(np.int64)
+    Lq = b.q_lens.astype(np.int64)
+    return int((Lq * P + Lq * (Lq + 1) // 2).sum())
+
+
+def prefill_flops(b: W.PagedBatch) -> int:
+    return 4 * 128 * b.num_q_heads * prefill_pairs(b)
+
+
+def source_hash(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "paged_kv_attention_store_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key: str, sources) -> float | None:
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_sha") != source_hash(*sources):
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_attention_store_gb300 as nv
+    from paged_kv_attention_store_gb300 import build as lib_build
+
+    lib_build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        return float(t.item())
+
+    pk, pk_kind = peaks()
+
+    # ---------------- decode phase: store + decode on the Qwen3-8B batch ----------------
+    db = W.qwen8_decode(seed=rank)
+    kc, vc = db.cache()
+    k_cache, v_cache = to_dev(kc), to_dev(vc)
+    del kc, vc
+    q, k_new, v_new = to_dev(db.q), to_dev(db.k_new), to_dev(db.v_new)
+    slots, bt, ctx = to_dev(db.slot_mapping), to_dev(db.block_tables), to_dev(db.seq_lens)
+    out = torch.empty_like(q)
+    maxc = int(db.seq_lens.max())
+    ws_bytes = nv.nv_paged_decode_workspace_size(db.num_seqs, db.num_q_heads, 128, maxc)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    d_err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def decode_step(ev=None):
+        nv.nv_store_kvcache(k_new, v_new, slots, k_cache, v_cache, d_err=d_err)
+        if ev is not None:
+            ev[0].record(stream)
+        nv.nv_paged_decode_attn(q, k_cache, v_cache, bt, ctx, db.scale, out=out, max_context_len=maxc, workspace=ws,
+                                d_err=d_err)
+        if ev is not None:
+            ev[1].record(stream)
+
+    launches_per_decode_step = 1 + 1 + (1 if ws_bytes > 0 else 0)
+
+    sampler = ClockSampler(local_rank)
+    sampler.__enter__()
+    try:
+        for _ in range(args.warmup):
+            decode_step()
+        barrier()
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            decode_step(kev[i])
+        t_end.record(stream)
+        barrier()
+        dec_ms = t_start.elapsed_time(t_end)
+        dec_kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+        assert int(d_err.item()) == 0, f"device error flags {int(d_err.item())}"
+
+        # e2e: the same step through the public API from pinned HOST buffers, inputs copied in
+        # and the output read back every step
+        h_q = torch.from_numpy(db.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_k = torch.from_numpy(db.k_new.view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_v = torch.from_numpy(db.v_new.view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_s = torch.from_numpy(db.slot_mapping).pin_memory()
+        h_bt = torch.from_numpy(db.block_tables).pin_memory()
+        h_ctx = torch.from_numpy(db.seq_lens).pin_memory()
+        h_out = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_s, h_bt, h_ctx))
+        d2h = h_out.numel() * h_out.element_size()
+
+        def e2e_step():
+            q.copy_(h_q, non_blocking=True)
+            k_new.copy_(h_k, non_blocking=True)
+            v_new.copy_(h_v, non_blocking=True)
+            slots.copy_(h_s, non_blocking=True)
+            bt.copy_(h_bt, non_blocking=True)
+            ctx.copy_(h_ctx, non_blocking=True)
+            decode_step()
+            h_out.copy_(out, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1)
+
+        # ---------------- prefill phase: store + prefill on the chunked-prefill batch ----------------
+        del k_cache, v_cache, ws
+        torch.cuda.empty_cache()
+        pb = W.prefill_chunk(seed=rank)
+        pkc, pvc = pb.cache()
+        pk_cache, pv_cache = to_dev(pkc), to_dev(pvc)
+        del pkc, pvc
+        pq, pk_new, pv_new = to_dev(pb.q), to_dev(pb.k_new), to_dev(pb.v_new)
+        pslots, pbt = to_dev(pb.slot_mapping), to_dev(pb.block_tables)
+        pcu_q, pcu_k = to_dev(pb.cu_seqlens_q), to_dev(pb.cu_seqlens_k)
+        pout = torch.empty_like(pq)
+        mq = int(pb.q_lens.max())
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > 129 MB L2
+
+        def prefill_step(ev=None):
+            if ev is not None:
+                ev[0].record(stream)
+            nv.nv_store_kvcache(pk_new, pv_new, pslots, pk_cache, pv_cache, d_err=d_err)
+            if ev is not None:
+                ev[1].record(stream)
+            nv.nv_paged_prefill_attn(pq, pk_cache, pv_cache, pcu_q, pcu_k, pbt, pb.scale, max_seqlen_q=mq, out=pout,
+                                     d_err=d_err)
+            if ev is not None:
+                ev[2].record(stream)
+
+        for _ in range(args.warmup):
+            prefill_step()
+        barrier()
+        pev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)          # L2 flush between steps, outside the step's events
+            prefill_step(pev[i])
+        barrier()
+        store_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in pev)
+        pf_ms = statistics.mean(b.elapsed_time(c) for _, b, c in pev)
+        pf_step_ms = statistics.mean(a.elapsed_time(c) for a, _, c in pev)
+        assert int(d_err.item()) == 0, f"device error flags {int(d_err.item())}"
+    finally:
+        sampler.__exit__(None, None, None)
+
+    dec_ms_max = max_over_ranks(dec_ms)
+    e2e_ms_max = max_over_ranks(e2e_ms)
+    dec_kernel_ms_max = max_over_ranks(dec_kernel_ms)
+    pf_ms_max = max_over_ranks(pf_ms)
+    pf_step_ms_max = max_over_ranks(pf_step_ms)
+    store_ms_max = max_over_ranks(store_ms)
+
+    kv_total = sum_over_ranks(float(decode_kv_bytes(db))) * args.steps
+    tok_total = sum_over_ranks(float(db.seq_lens.astype(np.int64).sum())) * args.steps
+    value = kv_total / (dec_ms_max * 1e-3) / 1e9
+    e2e_value = kv_total / (e2e_ms_max * 1e-3) / 1e9
+    alg_bytes = decode_algorithmic_bytes(db)
+    achieved = alg_bytes / (dec_kernel_ms_max * 1e-3) / 1e9
+    pf_flops_rank = prefill_flops(pb)
+    pf_flops = sum_over_ranks(float(pf_flops_rank))
+    pf_tflops = pf_flops / (pf_ms_max * 1e-3) / 1e12
+    pf_tflops_rank = pf_flops_rank / (pf_ms_max * 1e-3) / 1e12
+    pf_tok = sum_over_ranks(float(prefill_pairs(pb)))
+    store_bytes = 2 * 2 * int(pb.q_lens.sum()) * pb.num_kv_heads * 128 * 2     # read + write, K and V
+
+    if rank != 0:
+        return None
+    cpu = None if args.no_cpu_baseline else cpu_baseline_decode(db, args.cpu_seconds)
+    cpu_pf = None if args.no_cpu_baseline else cpu_baseline_prefill(pb, args.cpu_seconds)
+    clocks = sampler.summary()
+    hbm_peak = float(pk["hbm_gbs"])
+    tc_peak = float(pk["bf16_tflops"])
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dec_ms_max / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) values rounded to bf16, block tables dealt from a shuffled pool",
+        "config": {
+            "workload": "qwen3-8b-shaped decode step (store 512 new K/V rows + paged decode): 512 seqs, "
+                        "ctx U[1024,4096], 32 q / 8 kv heads, head_dim 128, block_size 256, 1 layer",
+            "num_seqs": db.num_seqs, "sum_context": int(db.seq_lens.sum()), "max_context": maxc,
+            "kv_bytes_per_step": decode_kv_bytes(db),
+            "l2": "inputs larger than L2 (decode KV 5.4 GB per step); L2 flushed between prefill steps",
+            "parallelism": f"replicas x{world} (each rank its own batch; no collective on the path)",
+        },
+        "hbm_frac_of_peak": round(value / hbm_peak, 4),
+        "attended_tok_s": round(tok_total / (dec_ms_max * 1e-3), 1),
+        "roofline": {
+            "kernel": "paged_decode_kernel + merge_splits_kernel (nv_paged_decode_attn)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4),
+            "peak_source": f"{pk_kind} hbm_gbs",
+            "algorithmic_bytes_per_launch": alg_bytes,
+            "traffic": profiled_traffic("decode_qwen8", ["paged_decode.cu", "nv_common.cuh"]),
+        },
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max / args.steps, 4)},
+        "gpu_launches": (launches_per_decode_step * 2 + 2) * args.steps,
+        "gpu_launches_note": "decode phase: store + split-KV decode + merge per step; "
+                             "e2e phase: same kernels; prefill phase: store + prefill per step",
+        "clocks": clocks,
+        "prefill": {
+            "workload": "chunked prefill with prefix cache (store 16384 new rows + causal varlen prefill): 16 seqs, "
+                        "prefixes 256*U{0..8}, chunks a uniform composition of 16384, 16 q / 8 kv heads, bs 256",
+            "value": round(pf_tflops, 1), "unit": "TFLOP/s",
+            "flops_per_step": pf_flops_rank, "causal_pairs_per_step": prefill_pairs(pb),
+            "ms_prefill_kernel": round(pf_ms_max, 4), "ms_per_step": round(pf_step_ms_max, 4),
+            "attended_pairs_s": round(pf_tok / (pf_ms_max * 1e-3), 1),
+            "roofline": {
+                "kernel": "paged_prefill_kernel (nv_paged_prefill_attn)",
+                "bound": "tensor", "achieved": round(pf_tflops_rank, 1), "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": round(pf_tflops_rank / tc_peak, 4), "peak_source": f"{pk_kind} bf16_tflops (burst)",
+                "traffic": profiled_traffic("prefill_chunk", ["paged_prefill.cu", "nv_common.cuh"]),
+            },
+            "store": {"ms": round(store_ms_max, 4), "gbs": round(store_bytes / (store_ms_max * 1e-3) / 1e9, 1),
+                      "bytes_per_step": store_bytes},
+            "cpu_baseline": cpu_pf,
+        },
+    }
+    return line
+
+
+# ----------------------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ----------------------------------------------------------------------------------------
+
+def cpu_baseline_decode(b: W.PagedBatch, seconds: float, max_seqs: int | None = None):
+    """Oracle decode, single thread, sequence by sequence until ~`seconds` of CPU work."""
+    import oracle
+    orc = oracle.default()
+    done, tokens, spent = 0, 0, 0.0
+    order = np.random.default_rng(7).permutation(b.num_seqs)
+    for s in order:
+        sub, ids = b.subset([int(s)])
+        kc, vc = sub.cache(ids, threads=1)
+        orc.store_kvcache(sub.k_new, sub.v_new, sub.slot_mapping, kc, vc)
+        t0 = time.perf_counter()
+        orc.decode_attn(sub.q, kc, vc, sub.block_tables, sub.context_lens, sub.num_kv_heads, sub.block_size,
+                        sub.scale, threads=1)
+        spent += time.perf_counter() - t0
+        done += 1
+        tokens += int(sub.seq_lens.sum())
+        if spent >= seconds or (max_seqs and done >= max_seqs):
+            break
+    kv = tokens * b.num_kv_heads * KV_BYTES_PER_TOKEN_PER_KVHEAD
+    return {"value": round(kv / spent / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {b.num_seqs} sequences ({tokens} attended positions x {b.num_q_heads} heads) "
+                      f"of the same decode batch, one thread, {spent:.1f} s",
+            "seconds": round(spent, 2), "attended_tok_s": round(tokens / spent, 1)}
+
+
+def cpu_baseline_prefill(b: W.PagedBatch, seconds: float):
+    """Oracle prefill, single thread, on a random sample of query rows until ~`seconds`."""
+    import oracle
+    orc = oracle.default()
+    kc, vc = b.cache(threads=1)
+    orc.store_kvcache(b.k_new, b.v_new, b.slot_mapping, kc, vc)
+    rows_all = np.random.default_rng(8).permutation(int(b.q_lens.sum()))
+    cu = b.cu_seqlens_q
+    P = b.meta["prefix_lens"]
+    spent, done, pairs, i = 0.0, 0, 0, 0
+    while spent < seconds and i < rows_all.size:
+        chunk = rows_all[i:i + 16]
+        i += 16
+        t0 = time.perf_counter()
+        orc.prefill_attn(b.q, kc, vc, b.cu_seqlens_q, b.cu_seqlens_k, b.block_tables, b.num_kv_heads,
+                         b.block_size, b.scale, rows=chunk, threads=1)
+        spent += time.perf_counter() - t0
+        for r in chunk:
+            s = int(np.searchsorted(cu, r, side="right") - 1)
+            pairs += int(P[s]) + int(r - cu[s]) + 1
+        done += chunk.size
+    flops = 4 * 128 * b.num_q_heads * pairs
+    return {"value": round(flops / spent / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {int(b.q_lens.sum())} query rows ({pairs} causal pairs x {b.num_q_heads} heads) "
+                      f"of the same prefill batch, one thread, {spent:.1f} s",
+            "seconds": round(spent, 2)}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm, on rank 0 only; other ranks exit without work."""
+    if rank != 0:
+        return None
+    db = W.qwen8_decode(seed=0)
+    per_step = max(1, int(args.ref_seqs_per_step))
+    # warm-up steps (untimed), then K timed steps, each a bounded sample of the batch
+    for _ in range(min(args.warmup, 1)):
+        cpu_baseline_decode(db, 0.0, max_seqs=1)
+    t0 = time.perf_counter()
+    kv = 0.0
+    spent = 0.0
+    toks = 0
+    for k in range(args.steps):
+        r = cpu_baseline_decode(db, 1e9, max_seqs=per_step)
+        spent += r["seconds"]
+        toks += int(r["attended_tok_s"] * r["seconds"])
+        kv += r["value"] * 1e9 * r["seconds"]
+    wall = time.perf_counter() - t0
+    value = kv / spent / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(spent / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic: seeded N(0,1) values rounded to bf16, block tables dealt from a shuffled pool",
+        "config": {"workload": "qwen3-8b-shaped decode step (store + paged decode), "
+                               f"{per_step} sampled sequence(s) per step", "num_seqs": db.num_seqs},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} sequence(s) of the 512-sequence batch per step, one thread"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": round(wall, 2),
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work per oracle baseline leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seqs-per-step", type=int, default=1)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend)
+    try:
+        line = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world,
+                                                                                         local_rank)
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
