@@ -491,6 +491,48 @@ def run_reference(args, rank, world):
     }
 
 
+def run_profile_case(case: str):
+    """Run one small case three times (store + attention) for an ncu capture, then exit.
+
+    decode-64seq: the first 64 sequences' shapes of the Qwen3-8B decode batch (about 0.7 GB of
+    KV, above the 129 MB L2, a few GB on the device in all); prefill-chunk: the full
+    chunked-prefill workload (about 0.3 GB)."""
+    import torch
+
+    import paged_kv_attention_store_gb300 as nv
+    from paged_kv_attention_store_gb300 import build as lib_build
+    lib_build.build()
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    if case == "decode-64seq":
+        ctx = np.random.default_rng([0, 200]).integers(1024, 4097, size=512)[:64]
+        b = W.make_decode("qwen3-8b-decode-64", 0, ctx, 32, 8, 128, 256)
+    else:
+        b = W.prefill_chunk()
+    kc, vc = b.cache()
+    k_cache, v_cache = to_dev(kc), to_dev(vc)
+    q, k_new, v_new, slots = to_dev(b.q), to_dev(b.k_new), to_dev(b.v_new), to_dev(b.slot_mapping)
+    bt, lens = to_dev(b.block_tables), to_dev(b.seq_lens)
+    cu_q, cu_k = to_dev(b.cu_seqlens_q), to_dev(b.cu_seqlens_k)
+    d_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        nv.nv_store_kvcache(k_new, v_new, slots, k_cache, v_cache, d_err=d_err)
+        if b.kind == "decode":
+            nv.nv_paged_decode_attn(q, k_cache, v_cache, bt, lens, b.scale, max_context_len=int(b.seq_lens.max()),
+                                    d_err=d_err)
+        else:
+            nv.nv_paged_prefill_attn(q, k_cache, v_cache, cu_q, cu_k, bt, b.scale, max_seqlen_q=int(b.q_lens.max()),
+                                     d_err=d_err)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": case, "d_err": int(d_err.item()),
+                      "algorithmic_bytes": decode_algorithmic_bytes(b) if b.kind == "decode" else None,
+                      "flops": prefill_flops(b) if b.kind == "prefill" else None}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -500,7 +542,12 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work per oracle baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seqs-per-step", type=int, default=1)
+    ap.add_argument("--profile-case", choices=["decode-64seq", "prefill-chunk"],
+                    help="run one small case three times for an ncu capture and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 

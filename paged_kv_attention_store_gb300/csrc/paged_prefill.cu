@@ -5,23 +5,27 @@
 // and Lk = cu_k[b+1]-cu_k[b] keys read through its block table; the first P = Lk-Lq were
 // cached before.  Query i of the chunk sees keys 0..P+i (bottom-right causal alignment).
 //
-// How (GB300 design; the pages call a library kernel here).  One CTA computes one 128-row
-// tile of one (sequence, kv head): with G = Hq/Hkv query heads per kv head, the tile packs
-// 128/G consecutive query tokens x G heads, so every K/V tile it loads serves all G heads.
-//   * warp 4 (TMA producer): K and V tiles of 128 keys x 128 dims come straight from the
-//     paged pool with 3-D tensor-map copies (dims: head_dim, kv head, slot) in 128-byte
-//     swizzled layout -- one box per block piece, so a 128-key tile costs one table lookup
-//     when block_size >= 128.  Two stages of K+V are in flight.
-//   * warp 5 (MMA issuer; also owns the tensor-memory allocation): one elected lane issues
-//     tcgen05.mma kind::f16 (bf16 operands from shared memory, fp32 accumulation in TMEM):
-//     S = Q K^T into one of two TMEM S buffers, then O += P V into the TMEM O accumulator.
-//     S(n+1) is issued before PV(n) so the tensor core works while softmax runs.
-//   * warps 0-3 (softmax / correction / epilogue): thread r owns tile row r = TMEM lane r.
-//     It reads its S row with tcgen05.ld, applies the causal mask only on tiles that cross
-//     the diagonal, keeps an online softmax in base 2 with a lazy rescale (the running max
-//     moves only when a score beats it by more than 8), writes P as bf16 into shared
-//     memory in the MMA's swizzled K-major layout, and -- rarely -- rescales its O row in
-//     TMEM.  At the end it normalises O and writes bf16 rows.
+// How (GB300 design; the pages call a library kernel here).  One CTA computes TWO 128-row
+// query tiles of one (sequence, kv head).  With G = Hq/Hkv query heads per kv head a tile
+// packs 128/G consecutive tokens x G heads, so every K/V tile loaded serves 2*G*(128/G) rows.
+//   * warp 8 (TMA producer): both Q tiles with one 3-D tensor-map copy each (dims head_dim,
+//     q head, token), then K and V tiles of 64 keys x 128 dims straight from the paged pool
+//     (dims head_dim, kv head, slot), 128-byte swizzled, into a 6-slot ring (K0 V0 K1 V1 ...),
+//     so loads run up to three key tiles ahead of the tensor core.
+//   * warps 9 and 10 (MMA issuers, one per query tile; warp 9 owns the tensor-memory
+//     allocation): one lane issues tcgen05.mma kind::f16 -- bf16 operands from shared
+//     memory, fp32 accumulators in TMEM.  For its tile i and key tile n it issues
+//     S_i(n+1) = Q_i K(n+1)^T into the other half of a double-buffered TMEM S tile BEFORE it
+//     waits for P_i(n), then O_i += P_i(n) V(n).  The two tiles' streams interleave on the
+//     tensor core, and each warpgroup finds its next S ready when it finishes a softmax.
+//   * warps 0-3 / 4-7 (softmax warpgroups, one per query tile): thread r owns row r = TMEM
+//     lane r.  It copies its 64 scores to registers with tcgen05.ld and frees the S buffer,
+//     masks only on tiles that cross the diagonal, keeps a base-2 online softmax with a lazy
+//     rescale (the running max moves only when a score beats it by more than 8, so O is
+//     rarely touched), writes P as bf16 into shared memory in the MMA's swizzled K-major
+//     layout (double-buffered), and at the end normalises O and stores bf16 rows.  A quarter
+//     of the exponentials run as a cubic polynomial on the FMA pipe (see exp2_poly3) so the
+//     two warpgroups do not queue on the special-function unit.
 // Every mbarrier wait is bounded; on timeout the kernel records NV_DERR_TIMEOUT and stops.
 #include <cuda.h>
 
@@ -34,36 +38,36 @@ namespace {
 using namespace nvkv;
 
 constexpr int kD = 128;
-constexpr int kBM = 128;            // tile rows (TMEM lanes)
-constexpr int kBN = 128;            // keys per KV tile
-constexpr int kStages = 2;          // K+V stages
-constexpr int kThreads = 192;       // warps 0-3 softmax, 4 producer, 5 MMA
-constexpr uint32_t kTmemCols = 512; // S0 [0,128), S1 [128,256), O [256,384)
+constexpr int kBM = 128;             // rows per query tile (TMEM lanes)
+constexpr int kBN = 64;              // keys per K/V tile
+constexpr int kSlots = 6;            // K/V ring slots
+constexpr int kThreads = 352;        // warps 0-3, 4-7 softmax; 8 producer; 9, 10 MMA
+constexpr uint32_t kTmemCols = 512;  // S[i][b] at i*128 + b*64; O[i] at 256 + i*128
 constexpr float kRescaleLog2 = 8.0f;
 
-constexpr uint32_t kHalfTile = kBM * 128;          // 128 rows x 128 bytes (64 bf16) = 16 KB
-constexpr uint32_t kTileBytes = 2 * kHalfTile;     // a 128 x 128 bf16 operand tile = 32 KB
-// shared memory layout (offsets from a 1024-aligned base)
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKV = kOffQ + kTileBytes;                    // stage s: K at +0, V at +kTileBytes
-constexpr uint32_t kOffP = kOffKV + kStages * 2 * kTileBytes;
-constexpr uint32_t kOffBar = kOffP + kTileBytes;
-constexpr uint32_t kNumBars = 1 + 3 * kStages + 2 + 2 + 1 + 1;
-constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kOffTmemSlot + 16 + 1024;          // + slack for 1024 alignment
+constexpr uint32_t kQHalf = kBM * 128;        // 128 rows x 64 dims bf16 = 16 KB
+constexpr uint32_t kQTile = 2 * kQHalf;       // 32 KB
+constexpr uint32_t kKVHalf = kBN * 128;       // 64 keys x 64 dims = 8 KB
+constexpr uint32_t kKVTile = 2 * kKVHalf;     // 16 KB
+constexpr uint32_t kPTile = kBM * 128;        // 128 rows x 64 keys bf16 = 16 KB
 
-// barrier indices
+constexpr uint32_t kOffQ = 0;                                   // Q[i] at i*kQTile
+constexpr uint32_t kOffP = kOffQ + 2 * kQTile;                  // P[i][b] at (2i+b)*kPTile
+constexpr uint32_t kOffKV = kOffP + 4 * kPTile;                 // slot s at s*kKVTile
+constexpr uint32_t kOffBar = kOffKV + kSlots * kKVTile;
+// barriers
 constexpr int kBarQ = 0;
-constexpr int kBarKFull = 1;                       // + stage
-constexpr int kBarVFull = kBarKFull + kStages;     // + stage
-constexpr int kBarKVEmpty = kBarVFull + kStages;   // + stage
-constexpr int kBarSFull = kBarKVEmpty + kStages;   // + (n & 1)
-constexpr int kBarSFree = kBarSFull + 2;           // + (n & 1)
-constexpr int kBarPFull = kBarSFree + 2;
-constexpr int kBarODone = kBarPFull + 1;
+constexpr int kBarKVFull = 1;                      // + slot
+constexpr int kBarKVEmpty = kBarKVFull + kSlots;   // + slot
+constexpr int kBarSFull = kBarKVEmpty + kSlots;    // + 2*i + b
+constexpr int kBarSFree = kBarSFull + 4;           // + 2*i + b
+constexpr int kBarPFull = kBarSFree + 4;           // + 2*i + b
+constexpr int kBarODone = kBarPFull + 4;           // + 2*i + b
+constexpr int kNumBars = kBarODone + 4;
+constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr uint32_t kSmemBytes = kOffTmemSlot + 16 + 1024;      // + slack for 1024-byte alignment
 
 struct PrefillParams {
-    const __nv_bfloat16 *q;
     __nv_bfloat16 *out;
     const int32_t *cu_q;
     const int32_t *cu_k;
@@ -71,80 +75,112 @@ struct PrefillParams {
     int32_t *d_err;
     int32_t bt_stride;
     int32_t num_q_heads;
-    int32_t num_kv_heads;
     int32_t group;          // G
     int32_t group_shift;    // log2 G
     int32_t block_shift;    // log2 block_size
-    int32_t box_rows;       // min(block_size, 128)
+    int32_t box_rows;       // min(block_size, kBN)
     int32_t num_blocks;
-    int32_t max_tiles;      // gridDim.x
+    int32_t max_pairs;      // gridDim.z
     float scale_log2;
 };
 
-// Offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a 128-byte-swizzled
-// [rows x 128 B] half tile: the chunk index is XOR-ed with the row's position in its 8-row group.
+// Offset of 16-byte chunk `chunk` (0..7) of row `row` in a [rows x 128 B] 128-byte-swizzled
+// operand: the chunk index is XOR-ed with the row's position inside its 8-row group.
 __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk)
 {
     return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
+// 2^x on the FMA pipe, for x <= 8 (scores minus a running max).  Range reduction: adding
+// 1.5 * 2^23 rounds x to the nearest integer j, held in the low mantissa bits of the sum;
+// f = x - j lies in [-0.5, 0.5] and 2^f comes from a cubic fitted to minimise the relative
+// error on that interval (max relative error 7.6e-5, well below the bf16 rounding of P);
+// finally j is added into the exponent field.  x is clamped at -126 so masked scores
+// (-inf) give a normal number of order 1e-38 instead of a wrapped exponent.
+__device__ __forceinline__ float exp2_poly3(float x)
+{
+    constexpr float kC0 = 0.9999282882344301f, kC1 = 0.6932609081979648f;
+    constexpr float kC2 = 0.24260776842531798f, kC3 = 0.05517030853684025f;
+    constexpr float kRound = 12582912.0f;
+    x = fmaxf(x, -126.0f);
+    const float y = __fadd_rn(x, kRound);
+    const float j = __fsub_rn(y, kRound);
+    const float f = __fsub_rn(x, j);
+    float q = fmaf(kC3, f, kC2);
+    q = fmaf(q, f, kC1);
+    q = fmaf(q, f, kC0);
+    return __uint_as_float(__float_as_uint(q) + (__float_as_uint(y) << 23));
+}
+
+__device__ __forceinline__ void tmem_ld32x2(uint32_t taddr, uint32_t (&r)[64])
+{
+    uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+    uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+    tmem_ld32(taddr, a);
+    tmem_ld32(taddr + 32, b);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                         const PrefillParams p)
+    paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                         const __grid_constant__ CUtensorMap tmap_v, const PrefillParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base = smem_u32(smem_raw);
-    const uint32_t base = (raw_base + 1023u) & ~1023u;     // SW128 tiles need 1024-byte alignment
+    const uint32_t base = (raw_base + 1023u) & ~1023u;     // swizzled tiles need 1024-byte alignment
     uint8_t *smem = smem_raw + (base - raw_base);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int b = blockIdx.z;
-    const int kvh = blockIdx.y;
+    const int kvh = blockIdx.x;
+    const int b = blockIdx.y;
 
-    // ---------------- per-tile geometry (uniform over the CTA) ----------------
+    // ---------------- work item geometry (uniform over the CTA) ----------------
     const int cq0 = __ldg(p.cu_q + b), cq1 = __ldg(p.cu_q + b + 1);
     const int ck0 = __ldg(p.cu_k + b), ck1 = __ldg(p.cu_k + b + 1);
     const int Lq = cq1 - cq0, Lk = ck1 - ck0;
     const int P = Lk - Lq;
-    const int tq = kBM >> p.group_shift;                  // query tokens per tile
     if (Lq < 0 || P < 0 || ((Lk + (1 << p.block_shift) - 1) >> p.block_shift) > p.bt_stride) {
-        if (blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0)
+        if (blockIdx.z == 0 && kvh == 0 && threadIdx.x == 0)
             flag_error(p.d_err, NV_DERR_LENGTH);
         return;
     }
-    const int ntiles = (Lq + tq - 1) / tq;
-    if (ntiles > p.max_tiles && blockIdx.x == 0 && kvh == 0 && threadIdx.x == 0)
+    const int tq = kBM >> p.group_shift;                   // query tokens per tile
+    const int npairs = (Lq + 2 * tq - 1) / (2 * tq);
+    if (npairs > p.max_pairs && blockIdx.z == 0 && kvh == 0 && threadIdx.x == 0)
         flag_error(p.d_err, NV_DERR_LENGTH);
-    const int tile = p.max_tiles - 1 - (int)blockIdx.x;  // heaviest tiles are dispatched first
-    if (tile >= ntiles)
+    const int pair = p.max_pairs - 1 - (int)blockIdx.z;    // the heaviest pairs are dispatched first
+    if (pair >= npairs)
         return;
-    const int i0 = tile * tq;
-    const int nq = min(tq, Lq - i0);
-    const int kv_len = P + i0 + nq;                        // keys any row of this tile can see
-    const int nkv = (kv_len + kBN - 1) / kBN;
-    const int first_masked = (P + i0 + 1) / kBN;           // tiles before this one need no mask
+    int i0[2], nq[2], nkv[2], first_masked[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        i0[i] = pair * 2 * tq + i * tq;
+        nq[i] = max(0, min(tq, Lq - i0[i]));
+        nkv[i] = nq[i] > 0 ? (P + i0[i] + nq[i] + kBN - 1) / kBN : 0;
+        first_masked[i] = (P + i0[i] + 1) / kBN;           // key tiles before this need no mask
+    }
+    const int kv_len = P + i0[nq[1] > 0 ? 1 : 0] + nq[nq[1] > 0 ? 1 : 0];   // keys any row can see
+    const int nkv_all = max(nkv[0], nkv[1]);
 
     const uint32_t bar = base + kOffBar;
     auto BAR = [&](int i) { return bar + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmemSlot);
 
     if (threadIdx.x == 0) {
-        mbar_init(BAR(kBarQ), 4);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(BAR(kBarKFull + s), 1);
-            mbar_init(BAR(kBarVFull + s), 1);
-            mbar_init(BAR(kBarKVEmpty + s), 1);
+        mbar_init(BAR(kBarQ), 1);
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(BAR(kBarKVFull + s), 1);
+            mbar_init(BAR(kBarKVEmpty + s), 2);    // one release per query tile's issuer
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < 4; ++s) {
             mbar_init(BAR(kBarSFull + s), 1);
             mbar_init(BAR(kBarSFree + s), 4);
+            mbar_init(BAR(kBarPFull + s), 4);
+            mbar_init(BAR(kBarODone + s), 1);
         }
-        mbar_init(BAR(kBarPFull), 4);
-        mbar_init(BAR(kBarODone), 1);
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -152,19 +188,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_o = tmem + 256;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // =========================== TMA producer ===========================
         if (lane == 0) {
+            prefetch_tmap(&tmap_q);
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
+            const uint32_t qbytes = (nq[1] > 0 ? 2u : 1u) * kQTile;
+            mbar_arrive_expect_tx(BAR(kBarQ), qbytes);
+            for (int i = 0; i < 2; ++i) {
+                if (nq[i] == 0)
+                    continue;
+                for (int h = 0; h < 2; ++h)
+                    tma_load_3d(base + kOffQ + i * kQTile + h * kQHalf, &tmap_q, h * 64, kvh * p.group, cq0 + i0[i],
+                                BAR(kBarQ));
+            }
             const int32_t *bt = p.block_tables + (size_t)b * p.bt_stride;
             const int bs_mask = (1 << p.block_shift) - 1;
             const int boxes = kBN / p.box_rows;
-            for (int n = 0; n < nkv; ++n) {
-                const int st = n % kStages;
-                if (n >= kStages && !mbar_wait(BAR(kBarKVEmpty + st), ((n / kStages) - 1) & 1)) {
+            for (int t = 0; t < 2 * nkv_all; ++t) {
+                const int n = t >> 1;
+                const int slot = t % kSlots;
+                if (t >= kSlots && !mbar_wait(BAR(kBarKVEmpty + slot), ((t / kSlots) - 1) & 1)) {
                     flag_error(p.d_err, NV_DERR_TIMEOUT);
                     break;
                 }
@@ -183,199 +229,203 @@ __global__ void __launch_bounds__(kThreads, 1)
                     slot0[k] = (blk << p.block_shift) + (j0 & bs_mask);
                     ++nbox;
                 }
-                const uint32_t bytes = (uint32_t)nbox * p.box_rows * 128u * 2u;
-                const uint32_t kdst = base + kOffKV + st * 2 * kTileBytes;
-                const uint32_t vdst = kdst + kTileBytes;
-                mbar_arrive_expect_tx(BAR(kBarKFull + st), bytes);
+                const CUtensorMap *map = (t & 1) ? &tmap_v : &tmap_k;
+                const uint32_t dst = base + kOffKV + slot * kKVTile;
+                mbar_arrive_expect_tx(BAR(kBarKVFull + slot), (uint32_t)nbox * p.box_rows * 128u * 2u);
                 for (int k = 0; k < boxes; ++k) {
                     if (slot0[k] < 0)
                         continue;
                     const uint32_t roff = (uint32_t)k * p.box_rows * 128u;
-                    tma_load_3d(kdst + roff, &tmap_k, 0, kvh, slot0[k], BAR(kBarKFull + st));
-                    tma_load_3d(kdst + kHalfTile + roff, &tmap_k, 64, kvh, slot0[k], BAR(kBarKFull + st));
-                }
-                mbar_arrive_expect_tx(BAR(kBarVFull + st), bytes);
-                for (int k = 0; k < boxes; ++k) {
-                    if (slot0[k] < 0)
-                        continue;
-                    const uint32_t roff = (uint32_t)k * p.box_rows * 128u;
-                    tma_load_3d(vdst + roff, &tmap_v, 0, kvh, slot0[k], BAR(kBarVFull + st));
-                    tma_load_3d(vdst + kHalfTile + roff, &tmap_v, 64, kvh, slot0[k], BAR(kBarVFull + st));
+                    tma_load_3d(dst + roff, map, 0, kvh, slot0[k], BAR(kBarKVFull + slot));
+                    tma_load_3d(dst + kKVHalf + roff, map, 64, kvh, slot0[k], BAR(kBarKVFull + slot));
                 }
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
-        // ============================ MMA issuer ============================
+    } else if (warp >= 9) {
+        // ================== MMA issuer for query tile i = warp - 9 ==================
         constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);   // Q, K both K-major
         constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kD, false, true);     // P K-major, V MN-major
-        bool ok = __all_sync(0xffffffffu, mbar_wait(BAR(kBarQ), 0));
-        tc_fence_after();
-        auto issue_pv = [&](int m) {
-            const int st = m % kStages;
-            ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarPFull), m & 1));
-            ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarVFull + st), (m / kStages) & 1));
+        const int i = warp - 9;
+        const int my_nkv = nkv[i];
+        const uint32_t qtile = base + kOffQ + i * kQTile;
+        const uint32_t o_tmem = tmem + 256 + i * 128;
+        bool ok = my_nkv == 0 || __all_sync(0xffffffffu, mbar_wait(BAR(kBarQ), 0));
+        auto issue_s = [&](int n) {
+            const int t = 2 * n;
+            const int slot = t % kSlots;
+            const int bb = n & 1;
+            ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarKVFull + slot), (t / kSlots) & 1));
+            if (n >= 2)
+                ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarSFree + 2 * i + bb), ((n - 2) >> 1) & 1));
             if (!ok)
                 return;
-            const uint32_t vtile = base + kOffKV + st * 2 * kTileBytes + kTileBytes;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t ktile = base + kOffKV + slot * kKVTile;
+                const uint32_t s_tmem = tmem + i * 128 + bb * 64;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    mma_bf16_ss(s_tmem, smem_desc_sw128(qtile + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024),
+                                smem_desc_sw128(ktile + (kk >> 2) * kKVHalf + (kk & 3) * 32, 16, 1024), idesc_s,
+                                kk > 0 ? 1u : 0u);
+                mma_commit(BAR(kBarSFull + 2 * i + bb));
+                mma_commit(BAR(kBarKVEmpty + slot));
+            }
+            __syncwarp();
+        };
+        auto issue_pv = [&](int m) {
+            const int t = 2 * m + 1;
+            const int slot = t % kSlots;
+            const int bb = m & 1;
+            ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarKVFull + slot), (t / kSlots) & 1));
+            if (!ok)
+                return;
+            const uint32_t vtile = base + kOffKV + slot * kKVTile;
             const int vrows = kv_len - m * kBN;
             if (vrows < kBN) {
-                // Keys past the sequence: their P is zero, but their V rows may hold anything
-                // (NaN patterns included) and 0 * NaN would poison O -- zero them.
-                const int nzero = (kBN - vrows) * 2 * 8;       // 16-byte chunks over both halves
-                for (int i = lane; i < nzero; i += 32) {
-                    const int half = i / ((kBN - vrows) * 8);
-                    const int rem = i % ((kBN - vrows) * 8);
-                    const uint32_t row = vrows + rem / 8;
-                    sts_u4(vtile + half * kHalfTile + row * 128u + (uint32_t)(rem % 8) * 16u, make_uint4(0, 0, 0, 0));
+                // Keys past the sequence carry P = 0, but their V rows may hold anything (NaN
+                // patterns included) and 0 * NaN would poison O: zero them.  Both issuers may
+                // do this for the last tile; they write the same zeros.
+                const int per_half = (kBN - vrows) * 8;        // 16-byte chunks
+                for (int c = lane; c < 2 * per_half; c += 32) {
+                    const int half = c / per_half;
+                    const int rem = c % per_half;
+                    sts_u4(vtile + half * kKVHalf + (uint32_t)(vrows + rem / 8) * 128u + (uint32_t)(rem % 8) * 16u,
+                           make_uint4(0, 0, 0, 0));
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
             }
+            ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarPFull + 2 * i + bb), (m >> 1) & 1));
+            if (!ok)
+                return;
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t ptile = base + kOffP;
+                const uint32_t ptile = base + kOffP + (2 * i + bb) * kPTile;
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t a = smem_desc_sw128(ptile + (kk >> 2) * kHalfTile + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bdesc = smem_desc_sw128(vtile + kk * 16 * 128, kHalfTile, 1024);
-                    mma_bf16_ss(tmem_o, a, bdesc, idesc_o, (m > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit(BAR(kBarODone));
-                mma_commit(BAR(kBarKVEmpty + st));
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    mma_bf16_ss(o_tmem, smem_desc_sw128(ptile + kk * 32, 16, 1024),
+                                smem_desc_sw128(vtile + kk * 16 * 128, kKVHalf, 1024), idesc_o,
+                                (m > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(BAR(kBarODone + 2 * i + bb));
+                mma_commit(BAR(kBarKVEmpty + slot));
             }
             __syncwarp();
         };
-        for (int n = 0; n < nkv && ok; ++n) {
-            const int st = n % kStages;
-            if (n >= 2)
-                ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarSFree + (n & 1)), ((n >> 1) - 1) & 1));
-            ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarKFull + st), (n / kStages) & 1));
-            if (!ok)
-                break;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t qtile = base + kOffQ;
-                const uint32_t ktile = base + kOffKV + st * 2 * kTileBytes;
-                const uint32_t s_tmem = tmem + (uint32_t)(n & 1) * kBN;
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kHalfTile + (kk & 3) * 32;
-                    mma_bf16_ss(s_tmem, smem_desc_sw128(qtile + off, 16, 1024), smem_desc_sw128(ktile + off, 16, 1024),
-                                idesc_s, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(BAR(kBarSFull + (n & 1)));
-            }
-            __syncwarp();
-            if (n >= 1)
-                issue_pv(n - 1);
+        if (my_nkv > 0)
+            issue_s(0);
+        for (int n = 0; n < my_nkv && ok; ++n) {
+            if (n + 1 < my_nkv)
+                issue_s(n + 1);      // the next scores are computed while this tile's softmax runs
+            issue_pv(n);
         }
-        if (ok && nkv >= 1)
-            issue_pv(nkv - 1);
+        // Key tiles this query tile never needs still count toward their slot's release: wait
+        // until the tile is loaded (so the arrival lands in the right phase), then arrive.
+        for (int t = 2 * my_nkv; t < 2 * nkv_all && ok; ++t) {
+            const int slot = t % kSlots;
+            ok = __all_sync(0xffffffffu, mbar_wait(BAR(kBarKVFull + slot), (t / kSlots) & 1));
+            if (ok && lane == 0)
+                mbar_arrive(BAR(kBarKVEmpty + slot));
+            __syncwarp();
+        }
         if (!ok && lane == 0)
             flag_error(p.d_err, NV_DERR_TIMEOUT);
     } else {
-        // ================= softmax / correction / epilogue (warps 0-3) =================
-        const int r = threadIdx.x;                    // tile row == TMEM lane
-        const int tok = i0 + (r >> p.group_shift);    // token index inside the chunk
-        const int head = kvh * p.group + (r & (p.group - 1));
+        // ============ softmax / correction / epilogue: warpgroup i owns query tile i ============
+        const int i = warp >> 2;
+        const int r = threadIdx.x & 127;                // tile row == TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t s_col = tmem + lane_base + i * 128;
+        const uint32_t o_addr = tmem + lane_base + 256 + i * 128;
+        const int tok = i0[i] + (r >> p.group_shift);   // token index inside the chunk
+        const int head = (int)kvh * p.group + (r & (p.group - 1));
         const bool valid = tok < Lq;
-        const int lim = P + tok;                      // last key this row may see
-
-        // ---- stage the Q tile (row r), 128-byte swizzled, zeros for rows past the chunk ----
-        {
-            const uint32_t qtile = base + kOffQ;
-            const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((size_t)(cq0 + tok) * p.num_q_heads + head) * kD);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-                sts_u4(qtile + (c >> 3) * kHalfTile + sw128(r, c & 7), v);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(BAR(kBarQ));
-        }
-
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const uint32_t ptile = base + kOffP;
-        float m_run = -INFINITY;   // running max of scale*log2(e)*s over this row
+        const int lim = P + tok;                        // last key this row may see
+        float m_run = -INFINITY;                        // running max of scale*log2(e)*s
         float l_run = 0.f;
         bool ok = true;
-        for (int n = 0; n < nkv; ++n) {
-            if (!__all_sync(0xffffffffu, mbar_wait(BAR(kBarSFull + (n & 1)), (n >> 1) & 1))) {
+        const int n_end = nkv[i];
+        for (int n = 0; n < n_end && ok; ++n) {
+            const int bb = n & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(kBarSFull + 2 * i + bb), (n >> 1) & 1))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t s_addr = tmem + lane_base + (uint32_t)(n & 1) * kBN;
-            const bool masked = n >= first_masked;
-            const int kbase = n * kBN;
-            // pass 1: row max of the (masked) raw scores
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(s_addr + c * 32, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float s = __uint_as_float(v[i]);
-                    const bool keep = !masked || (kbase + c * 32 + i <= lim);
-                    mx = keep ? fmaxf(mx, s) : mx;
-                }
-            }
-            const float mx2 = mx * p.scale_log2;
-            const bool need = mx2 > m_run + kRescaleLog2;
-            const float m_new = need ? mx2 : m_run;
-            const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;
-            // P buffer and O are free once PV(n-1) has completed
-            if (n >= 1 && !__all_sync(0xffffffffu, mbar_wait(BAR(kBarODone), (n - 1) & 1))) {
-                ok = false;
-                break;
-            }
-            // pass 2: p = 2^(s*scale*log2e - m), row sum, bf16 P into shared memory
-            float rs = 0.f;
-            const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
-#pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(s_addr + c * 32, v);
-                tmem_wait_ld();
-                uint32_t packed[16];
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const bool k0 = !masked || (kbase + c * 32 + i <= lim);
-                    const bool k1 = !masked || (kbase + c * 32 + i + 1 <= lim);
-                    const float p0 = k0 ? fast_exp2(fmaf(__uint_as_float(v[i]), p.scale_log2, neg_m)) : 0.f;
-                    const float p1 = k1 ? fast_exp2(fmaf(__uint_as_float(v[i + 1]), p.scale_log2, neg_m)) : 0.f;
-                    rs += p0 + p1;
-                    packed[i >> 1] = pack_bf16x2(p0, p1);
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t chunk = (uint32_t)(c * 4 + k);          // 16-byte chunk of the 128-key row
-                    const uint32_t addr = ptile + (chunk >> 3) * kHalfTile + sw128((uint32_t)r, chunk & 7);
-                    sts_u4(addr, make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]));
-                }
-            }
+            uint32_t sv[64];
+            tmem_ld32x2(s_col + bb * 64, sv);
+            tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(BAR(kBarSFree + (n & 1)));
+                mbar_arrive(BAR(kBarSFree + 2 * i + bb));
+            float s[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+                s[j] = __uint_as_float(sv[j]);
+            if (n >= first_masked[i]) {
+                const int rel = lim - n * kBN;          // keys j <= rel are visible
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                    s[j] = (j <= rel) ? s[j] : -INFINITY;
+            }
+            // row max: a tree, so the compare chain is 6 deep instead of 64
+            float mx8[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                mx8[j] = fmaxf(fmaxf(fmaxf(s[j], s[j + 8]), fmaxf(s[j + 16], s[j + 24])),
+                               fmaxf(fmaxf(s[j + 32], s[j + 40]), fmaxf(s[j + 48], s[j + 56])));
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            const float mx2 = mx * p.scale_log2;
+            const bool need = mx2 > m_run + kRescaleLog2;
+            const float m_new = need ? mx2 : m_run;
+            const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;   // m_run = -inf -> 0
+            const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
+            uint32_t pk[32];
+            float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < 64; j += 2) {
+                // every fourth pair on the FMA pipe, the rest on the special-function unit
+                const bool poly = ((j >> 1) & 3) == 3;
+                const float x0 = fmaf(s[j], p.scale_log2, neg_m);
+                const float x1 = fmaf(s[j + 1], p.scale_log2, neg_m);
+                const float p0 = poly ? exp2_poly3(x0) : fast_exp2(x0);
+                const float p1 = poly ? exp2_poly3(x1) : fast_exp2(x1);
+                rs8[(j >> 1) & 7] += p0 + p1;
+                pk[j >> 1] = pack_bf16x2(p0, p1);
+            }
+            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
             l_run = l_run * alpha + rs;
             m_run = m_new;
-            // rare: rescale this row's O accumulator (nothing to rescale before the first PV)
+            // P buffer bb is free once PV_i(n-2) has completed
+            if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(BAR(kBarODone + 2 * i + bb), ((n - 2) >> 1) & 1))) {
+                ok = false;
+                break;
+            }
+            const uint32_t ptile = base + kOffP + (2 * i + bb) * kPTile;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                sts_u4(ptile + sw128((uint32_t)r, (uint32_t)c),
+                       make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
+            // rare: rescale this row's O (PV_i(n-1) must be complete first; nothing to do at n = 0)
             if (n >= 1 && __any_sync(0xffffffffu, need)) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(BAR(kBarODone + 2 * i + ((n - 1) & 1)), ((n - 1) >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < kD / 32; ++c) {
                     uint32_t v[32];
-                    tmem_ld32(tmem_o + lane_base + c * 32, v);
+                    tmem_ld32(o_addr + c * 32, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                    tmem_st32(tmem_o + lane_base + c * 32, v);
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+                    tmem_st32(o_addr + c * 32, v);
                 }
                 tmem_wait_st();
             }
@@ -383,39 +433,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(BAR(kBarPFull));
+                mbar_arrive(BAR(kBarPFull + 2 * i + bb));
         }
         // ---- epilogue: O / l -> bf16 rows ----
-        if (ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarODone), (nkv - 1) & 1))) {
-            tc_fence_after();
-            const float inv = (valid && l_run > 0.f) ? 1.f / l_run : 0.f;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(cq0 + tok) * p.num_q_heads + head) * kD);
+        if (n_end > 0) {
+            const int last = n_end - 1;
+            if (ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarODone + 2 * i + (last & 1)), (last >> 1) & 1))) {
+                tc_fence_after();
+                const float inv = (valid && l_run > 0.f) ? 1.f / l_run : 0.f;
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(cq0 + tok) * p.num_q_heads + head) * kD);
 #pragma unroll
-            for (int c = 0; c < kD / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem_o + lane_base + c * 32, v);
-                tmem_wait_ld();
-                if (valid) {
+                for (int c = 0; c < kD / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(o_addr + c * 32, v);
+                    tmem_wait_ld();
+                    if (valid) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv, __uint_as_float(v[8 * k + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv);
-                        dst[c * 4 + k] = w;
+                        for (int k = 0; k < 4; ++k) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv, __uint_as_float(v[8 * k + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv);
+                            dst[c * 4 + k] = w;
+                        }
                     }
                 }
+            } else if (lane == 0) {
+                flag_error(p.d_err, NV_DERR_TIMEOUT);
             }
-        } else if (lane == 0) {
-            flag_error(p.d_err, NV_DERR_TIMEOUT);
         }
     }
 
-    // ---------------- teardown: every TMEM read is done before the free ----------------
+    // ---------------- teardown: every TMEM access is done before the free ----------------
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -443,18 +496,18 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// Pool [num_slots, Hkv, 128] bf16 seen as a 3-D tensor (dim0 = head_dim, dim1 = kv head,
-// dim2 = slot); a box is 64 dims x 1 head x box_rows slots, 128-byte swizzled.
-bool make_pool_map(CUtensorMap *map, const void *pool, int64_t num_slots, int num_kv_heads, int box_rows)
+// A [rows, heads, 128] bf16 tensor seen as 3-D (dim0 = head_dim, dim1 = head, dim2 = row); a box
+// is 64 dims x box_heads heads x box_rows rows, 128-byte swizzled.  Rows past the end read zeros.
+bool make_map(CUtensorMap *map, const void *base, int64_t rows, int heads, int box_heads, int box_rows)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
         return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)num_kv_heads, (cuuint64_t)num_slots};
-    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)num_kv_heads * kD * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)heads * kD * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box, estr,
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -493,14 +546,15 @@ extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const v
         return NV_ERR_SHAPE;
 
     const int box_rows = block_size < kBN ? block_size : kBN;
-    CUtensorMap tk, tv;
+    const int tq = kBM / group;
+    CUtensorMap tq_map, tk, tv;
     const int64_t num_slots = (int64_t)num_blocks * block_size;
-    if (!make_pool_map(&tk, k_cache, num_slots, num_kv_heads, box_rows) ||
-        !make_pool_map(&tv, v_cache, num_slots, num_kv_heads, box_rows))
+    if (!make_map(&tq_map, q, total_q, num_q_heads, group, tq) ||
+        !make_map(&tk, k_cache, num_slots, num_kv_heads, 1, box_rows) ||
+        !make_map(&tv, v_cache, num_slots, num_kv_heads, 1, box_rows))
         return NV_ERR_CUDA;
 
     PrefillParams p{};
-    p.q = static_cast<const __nv_bfloat16 *>(q);
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.cu_q = cu_seqlens_q;
     p.cu_k = cu_seqlens_k;
@@ -508,15 +562,15 @@ extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const v
     p.d_err = d_err;
     p.bt_stride = bt_stride;
     p.num_q_heads = num_q_heads;
-    p.num_kv_heads = num_kv_heads;
     p.group = group;
     p.group_shift = ilog2(group);
     p.block_shift = ilog2(block_size);
     p.box_rows = box_rows;
     p.num_blocks = num_blocks;
-    const int tq = kBM / group;
-    p.max_tiles = (max_seqlen_q + tq - 1) / tq;
+    p.max_pairs = (max_seqlen_q + 2 * tq - 1) / (2 * tq);
     p.scale_log2 = scale * nvkv::kLog2e;
+    if (p.max_pairs > 65535)
+        return NV_ERR_UNSUPPORTED;
 
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
@@ -525,7 +579,7 @@ extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const v
     });
     if (attr_err != cudaSuccess)
         return NV_ERR_CUDA;
-    dim3 grid(p.max_tiles, num_kv_heads, num_seqs);
-    paged_prefill_kernel<<<grid, kThreads, kSmemBytes, (cudaStream_t)stream>>>(tk, tv, p);
+    dim3 grid(num_kv_heads, num_seqs, p.max_pairs);
+    paged_prefill_kernel<<<grid, kThreads, kSmemBytes, (cudaStream_t)stream>>>(tq_map, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
