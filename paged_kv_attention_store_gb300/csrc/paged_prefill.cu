@@ -7,25 +7,28 @@
 //
 // How (GB300 design; the pages call a library kernel here).  One CTA computes TWO 128-row
 // query tiles of one (sequence, kv head).  With G = Hq/Hkv query heads per kv head a tile
-// packs 128/G consecutive tokens x G heads, so every K/V tile loaded serves 2*G*(128/G) rows.
-//   * warp 8 (TMA producer): both Q tiles with one 3-D tensor-map copy each (dims head_dim,
-//     q head, token), then K and V tiles of 64 keys x 128 dims straight from the paged pool
-//     (dims head_dim, kv head, slot), 128-byte swizzled, into a 6-slot ring (K0 V0 K1 V1 ...),
-//     so loads run up to three key tiles ahead of the tensor core.
-//   * warps 9 and 10 (MMA issuers, one per query tile; warp 9 owns the tensor-memory
-//     allocation): one lane issues tcgen05.mma kind::f16 -- bf16 operands from shared
-//     memory, fp32 accumulators in TMEM.  For its tile i and key tile n it issues
-//     S_i(n+1) = Q_i K(n+1)^T into the other half of a double-buffered TMEM S tile BEFORE it
-//     waits for P_i(n), then O_i += P_i(n) V(n).  The two tiles' streams interleave on the
-//     tensor core, and each warpgroup finds its next S ready when it finishes a softmax.
+// packs 128/G consecutive tokens x G heads, so every K/V tile loaded serves 256 query rows.
+// Key tiles are 128 keys: on GB300 an M=128 tcgen05.mma costs about the same ~96 cycles for
+// N=64 as for N=128, so narrower tiles leave most of the tensor core idle.
+//   * warp 8 (TMA producer): both Q tiles with one 3-D tensor-map copy per 64-dim half
+//     (dims head_dim, q head, token), then K and V tiles (128 keys x 128 dims) straight from
+//     the paged pool (dims head_dim, kv head, slot), 128-byte swizzled, into a 5-slot ring
+//     K0 V0 K1 V1 ...; the sequence's block-table row is held 32 entries at a time in the
+//     warp's registers, so a copy never waits on a dependent table load.
+//   * warp 9 (MMA issuer; owns the TMEM allocation): one lane issues tcgen05.mma kind::f16
+//     with fp32 accumulators in tensor memory: S_i(n) = Q_i K(n)^T (both operands from
+//     shared memory) and O_i += P_i(n) V(n) with P_i read from TENSOR memory, where the
+//     softmax wrote it over S_i.  The issue order S_0(n), S_1(n), PV_0(n), PV_1(n) makes the
+//     two tiles alternate: one tile's products run on the tensor core while the other tile's
+//     softmax runs.  (Issued independently, the tiles fall into lockstep, and the tensor core
+//     and the exp unit each sit idle half the time.)
 //   * warps 0-3 / 4-7 (softmax warpgroups, one per query tile): thread r owns row r = TMEM
-//     lane r.  It copies its 64 scores to registers with tcgen05.ld and frees the S buffer,
-//     masks only on tiles that cross the diagonal, keeps a base-2 online softmax with a lazy
-//     rescale (the running max moves only when a score beats it by more than 8, so O is
-//     rarely touched), writes P as bf16 into shared memory in the MMA's swizzled K-major
-//     layout (double-buffered), and at the end normalises O and stores bf16 rows.  A quarter
-//     of the exponentials run as a cubic polynomial on the FMA pipe (see exp2_poly3) so the
-//     two warpgroups do not queue on the special-function unit.
+//     lane r.  It reads its 128 scores in two 64-column halves, computes the exponentials
+//     against the running max while the tile max forms (a row is redone only when the max
+//     moves past the lazy-rescale threshold of 2^8, i.e. almost only on the first tile),
+//     masks only on tiles that cross the diagonal, writes P as bf16 pairs back into the S
+//     columns (tcgen05.st), rescales O in TMEM in the rare moved-max case, and at the end
+//     normalises O and stores bf16 rows.
 // Every mbarrier wait is bounded; on timeout the kernel records NV_DERR_TIMEOUT and stops.
 #include <cuda.h>
 
@@ -39,31 +42,30 @@ using namespace nvkv;
 
 constexpr int kD = 128;
 constexpr int kBM = 128;             // rows per query tile (TMEM lanes)
-constexpr int kBN = 64;              // keys per K/V tile
-constexpr int kSlots = 6;            // K/V ring slots
-constexpr int kThreads = 352;        // warps 0-3, 4-7 softmax; 8 producer; 9, 10 MMA
-constexpr uint32_t kTmemCols = 512;  // S[i][b] at i*128 + b*64; O[i] at 256 + i*128
+constexpr int kBN = 128;             // keys per K/V tile
+constexpr int kSlots = 5;            // K/V ring slots
+constexpr int kThreads = 320;        // warps 0-3, 4-7 softmax; 8 producer; 9 MMA
+constexpr uint32_t kTmemCols = 512;  // tile i: S_i / P_i at i*256 + [0, 128), O_i at i*256 + [128, 256)
 constexpr float kRescaleLog2 = 8.0f;
+// Of every 8 score pairs, this many take the polynomial exp2 on the FMA pipe; the rest use the
+// special-function unit.
+#ifndef NVKV_PREFILL_POLY_PAIRS
+#define NVKV_PREFILL_POLY_PAIRS 0
+#endif
+constexpr int kPolyPairs = NVKV_PREFILL_POLY_PAIRS;
 
-constexpr uint32_t kQHalf = kBM * 128;        // 128 rows x 64 dims bf16 = 16 KB
-constexpr uint32_t kQTile = 2 * kQHalf;       // 32 KB
-constexpr uint32_t kKVHalf = kBN * 128;       // 64 keys x 64 dims = 8 KB
-constexpr uint32_t kKVTile = 2 * kKVHalf;     // 16 KB
-constexpr uint32_t kPTile = kBM * 128;        // 128 rows x 64 keys bf16 = 16 KB
-
-constexpr uint32_t kOffQ = 0;                                   // Q[i] at i*kQTile
-constexpr uint32_t kOffP = kOffQ + 2 * kQTile;                  // P[i][b] at (2i+b)*kPTile
-constexpr uint32_t kOffKV = kOffP + 4 * kPTile;                 // slot s at s*kKVTile
-constexpr uint32_t kOffBar = kOffKV + kSlots * kKVTile;
-// barriers
+constexpr uint32_t kHalf = 128 * 128;         // 128 rows x 64 dims bf16 (one swizzle atom wide) = 16 KB
+constexpr uint32_t kTile = 2 * kHalf;         // a 128 x 128 bf16 operand = 32 KB
+constexpr uint32_t kOffQ = 0;                 // Q[i] at i*kTile
+constexpr uint32_t kOffKV = 2 * kTile;        // slot s at s*kTile
+constexpr uint32_t kOffBar = kOffKV + kSlots * kTile;
 constexpr int kBarQ = 0;
 constexpr int kBarKVFull = 1;                      // + slot
 constexpr int kBarKVEmpty = kBarKVFull + kSlots;   // + slot
-constexpr int kBarSFull = kBarKVEmpty + kSlots;    // + 2*i + b
-constexpr int kBarSFree = kBarSFull + 4;           // + 2*i + b
-constexpr int kBarPFull = kBarSFree + 4;           // + 2*i + b
-constexpr int kBarODone = kBarPFull + 4;           // + 2*i + b
-constexpr int kNumBars = kBarODone + 4;
+constexpr int kBarSFull = kBarKVEmpty + kSlots;    // + i
+constexpr int kBarPFull = kBarSFull + 2;           // + i
+constexpr int kBarODone = kBarPFull + 2;           // + i
+constexpr int kNumBars = kBarODone + 2;
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffTmemSlot + 16 + 1024;      // + slack for 1024-byte alignment
 
@@ -84,40 +86,111 @@ struct PrefillParams {
     float scale_log2;
 };
 
-// Offset of 16-byte chunk `chunk` (0..7) of row `row` in a [rows x 128 B] 128-byte-swizzled
-// operand: the chunk index is XOR-ed with the row's position inside its 8-row group.
-__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk)
+// ---- packed fp32x2 arithmetic (Blackwell: one instruction for two fp32 lanes) ----
+__device__ __forceinline__ uint64_t f2_pack(float a, float b)
 {
-    return row * 128u + ((chunk ^ (row & 7u)) << 4);
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &a, float &b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
-// 2^x on the FMA pipe, for x <= 8 (scores minus a running max).  Range reduction: adding
-// 1.5 * 2^23 rounds x to the nearest integer j, held in the low mantissa bits of the sum;
-// f = x - j lies in [-0.5, 0.5] and 2^f comes from a cubic fitted to minimise the relative
-// error on that interval (max relative error 7.6e-5, well below the bf16 rounding of P);
-// finally j is added into the exponent field.  x is clamped at -126 so masked scores
-// (-inf) give a normal number of order 1e-38 instead of a wrapped exponent.
-__device__ __forceinline__ float exp2_poly3(float x)
+// 2^x0, 2^x1 on the FMA pipe (packed fp32x2), for x <= 8 (scores minus a running max).
+// Range reduction: adding 1.5 * 2^23 rounds x to the nearest integer j, held in the low
+// mantissa bits of the sum; f = x - j lies in [-0.5, 0.5] and 2^f comes from a cubic fitted to
+// minimise the relative error on that interval (max relative error 7.6e-5, well below the bf16
+// rounding of P); finally j is added into the exponent field.  x is clamped at -126 so masked
+// scores (-inf) give a normal number of order 1e-38 instead of a wrapped exponent.
+__device__ __forceinline__ void exp2_poly3_x2(float x0, float x1, float &p0, float &p1)
 {
     constexpr float kC0 = 0.9999282882344301f, kC1 = 0.6932609081979648f;
     constexpr float kC2 = 0.24260776842531798f, kC3 = 0.05517030853684025f;
     constexpr float kRound = 12582912.0f;
-    x = fmaxf(x, -126.0f);
-    const float y = __fadd_rn(x, kRound);
-    const float j = __fsub_rn(y, kRound);
-    const float f = __fsub_rn(x, j);
-    float q = fmaf(kC3, f, kC2);
-    q = fmaf(q, f, kC1);
-    q = fmaf(q, f, kC0);
-    return __uint_as_float(__float_as_uint(q) + (__float_as_uint(y) << 23));
+    const uint64_t x = f2_pack(fmaxf(x0, -126.0f), fmaxf(x1, -126.0f));
+    const uint64_t y = f2_add(x, f2_pack(kRound, kRound));
+    const uint64_t j = f2_add(y, f2_pack(-kRound, -kRound));
+    const uint64_t f = f2_fma(j, f2_pack(-1.0f, -1.0f), x);
+    uint64_t q = f2_fma(f2_pack(kC3, kC3), f, f2_pack(kC2, kC2));
+    q = f2_fma(q, f, f2_pack(kC1, kC1));
+    q = f2_fma(q, f, f2_pack(kC0, kC0));
+    float q0, q1, y0, y1;
+    f2_unpack(q, q0, q1);
+    f2_unpack(y, y0, y1);
+    p0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(y0) << 23));
+    p1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(y1) << 23));
 }
 
-__device__ __forceinline__ void tmem_ld32x2(uint32_t taddr, uint32_t (&r)[64])
+// Max of 64 scores with 3-input max (32 instructions, 4 levels deep).
+__device__ __forceinline__ float max64(const float (&s)[64])
 {
-    uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
-    uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
-    tmem_ld32(taddr, a);
-    tmem_ld32(taddr + 32, b);
+    float m22[22];
+#pragma unroll
+    for (int k = 0; k < 21; ++k)
+        m22[k] = fmax3(s[3 * k], s[3 * k + 1], s[3 * k + 2]);
+    m22[21] = s[63];
+    float m8[8];
+#pragma unroll
+    for (int k = 0; k < 7; ++k)
+        m8[k] = fmax3(m22[3 * k], m22[3 * k + 1], m22[3 * k + 2]);
+    m8[7] = m22[21];
+    return fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+}
+
+// p = 2^(s * scale_log2 + neg_m) for 64 scores -> 32 bf16 pairs in pk; returns the fp32 sum.
+__device__ __forceinline__ float exp_pack64(const float (&s)[64], float scale_log2, float neg_m, uint32_t *pk)
+{
+    const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
+    const uint64_t negm2 = f2_pack(neg_m, neg_m);
+    uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        float x0, x1, p0, p1;
+        f2_unpack(f2_fma(f2_pack(s[2 * k], s[2 * k + 1]), scale2, negm2), x0, x1);
+        if ((k & 7) >= 8 - kPolyPairs) {
+            exp2_poly3_x2(x0, x1, p0, p1);
+        } else {
+            p0 = fast_exp2(x0);
+            p1 = fast_exp2(x1);
+        }
+        rs2[k & 3] = f2_add(rs2[k & 3], f2_pack(p0, p1));
+        pk[k] = pack_bf16x2(p0, p1);
+    }
+    float ra, rb, rc, rd;
+    f2_unpack(f2_add(rs2[0], rs2[1]), ra, rb);
+    f2_unpack(f2_add(rs2[2], rs2[3]), rc, rd);
+    return (ra + rb) + (rc + rd);
+}
+
+// Load 64 score columns of this thread's row and apply the causal mask (keys j > rel hidden).
+__device__ __forceinline__ void load_scores(uint32_t taddr, bool masked, int rel, float (&s)[64])
+{
+    uint32_t v[64];
+    tmem_ld64(taddr, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 64; ++j)
+        s[j] = (!masked || j <= rel) ? __uint_as_float(v[j]) : -INFINITY;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -170,11 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(BAR(kBarQ), 1);
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(BAR(kBarKVFull + s), 1);
-            mbar_init(BAR(kBarKVEmpty + s), 2);    // one release per query tile's issuer
+            mbar_init(BAR(kBarKVEmpty + s), 1);
         }
-        for (int s = 0; s < 4; ++s) {
+        for (int s = 0; s < 2; ++s) {
             mbar_init(BAR(kBarSFull + s), 1);
-            mbar_init(BAR(kBarSFree + s), 4);
             mbar_init(BAR(kBarPFull + s), 4);
             mbar_init(BAR(kBarODone + s), 1);
         }
@@ -195,139 +267,154 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tmap_q);
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
-            const uint32_t qbytes = (nq[1] > 0 ? 2u : 1u) * kQTile;
-            mbar_arrive_expect_tx(BAR(kBarQ), qbytes);
+            mbar_arrive_expect_tx(BAR(kBarQ), (nq[1] > 0 ? 2u : 1u) * kTile);
             for (int i = 0; i < 2; ++i) {
                 if (nq[i] == 0)
                     continue;
                 for (int h = 0; h < 2; ++h)
-                    tma_load_3d(base + kOffQ + i * kQTile + h * kQHalf, &tmap_q, h * 64, kvh * p.group, cq0 + i0[i],
+                    tma_load_3d(base + kOffQ + i * kTile + h * kHalf, &tmap_q, h * 64, kvh * p.group, cq0 + i0[i],
                                 BAR(kBarQ));
             }
-            const int32_t *bt = p.block_tables + (size_t)b * p.bt_stride;
-            const int bs_mask = (1 << p.block_shift) - 1;
-            const int boxes = kBN / p.box_rows;
-            for (int t = 0; t < 2 * nkv_all; ++t) {
-                const int n = t >> 1;
+        }
+        const int32_t *bt = p.block_tables + (size_t)b * p.bt_stride;
+        const int nblk = (kv_len + (1 << p.block_shift) - 1) >> p.block_shift;   // entries this CTA reads
+        const int bs_mask = (1 << p.block_shift) - 1;
+        const int boxes = kBN / p.box_rows;
+        int win_base = 0;
+        int win = lane < nblk ? __ldg(bt + lane) : -1;
+        bool ok = true;
+        for (int n = 0; n < nkv_all && ok; ++n) {
+            int slot0[kBN / 16];                    // first slot of each box; -1 = skip the box
+            int nbox = 0;
+            for (int k = 0; k < boxes; ++k) {
+                const int j0 = n * kBN + k * p.box_rows;
+                slot0[k] = -1;
+                if (j0 >= kv_len)
+                    continue;
+                const int lb = j0 >> p.block_shift;
+                if (lb >= win_base + 32) {          // advance the window (warp-uniform)
+                    win_base = lb & ~31;
+                    win = win_base + lane < nblk ? __ldg(bt + win_base + lane) : -1;
+                }
+                const int blk = __shfl_sync(0xffffffffu, win, lb - win_base);
+                if (blk < 0 || blk >= p.num_blocks) {
+                    if (lane == 0)
+                        flag_error(p.d_err, NV_DERR_BLOCK_RANGE);
+                    continue;
+                }
+                slot0[k] = (blk << p.block_shift) + (j0 & bs_mask);
+                ++nbox;
+            }
+            const uint32_t bytes = (uint32_t)nbox * p.box_rows * 128u * 2u;
+            for (int kv = 0; kv < 2; ++kv) {        // K(n) then V(n): tiles t = 2n, 2n+1
+                const int t = 2 * n + kv;
                 const int slot = t % kSlots;
-                if (t >= kSlots && !mbar_wait(BAR(kBarKVEmpty + slot), ((t / kSlots) - 1) & 1)) {
-                    flag_error(p.d_err, NV_DERR_TIMEOUT);
+                if (t >= kSlots &&
+                    !__all_sync(0xffffffffu, mbar_wait(BAR(kBarKVEmpty + slot), ((t / kSlots) - 1) & 1))) {
+                    if (lane == 0)
+                        flag_error(p.d_err, NV_DERR_TIMEOUT);
+                    ok = false;
                     break;
                 }
-                int slot0[kBN / 16];
-                int nbox = 0;
-                for (int k = 0; k < boxes; ++k) {
-                    const int j0 = n * kBN + k * p.box_rows;
-                    slot0[k] = -1;
-                    if (j0 >= kv_len)
-                        continue;
-                    const int blk = __ldg(bt + (j0 >> p.block_shift));
-                    if (blk < 0 || blk >= p.num_blocks) {
-                        flag_error(p.d_err, NV_DERR_BLOCK_RANGE);
-                        continue;
+                if (lane == 0) {
+                    const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
+                    const uint32_t dst = base + kOffKV + slot * kTile;
+                    mbar_arrive_expect_tx(BAR(kBarKVFull + slot), bytes);
+                    for (int k = 0; k < boxes; ++k) {
+                        if (slot0[k] < 0)
+                            continue;
+                        const uint32_t roff = (uint32_t)k * p.box_rows * 128u;
+                        tma_load_3d(dst + roff, map, 0, kvh, slot0[k], BAR(kBarKVFull + slot));
+                        tma_load_3d(dst + kHalf + roff, map, 64, kvh, slot0[k], BAR(kBarKVFull + slot));
                     }
-                    slot0[k] = (blk << p.block_shift) + (j0 & bs_mask);
-                    ++nbox;
                 }
-                const CUtensorMap *map = (t & 1) ? &tmap_v : &tmap_k;
-                const uint32_t dst = base + kOffKV + slot * kKVTile;
-                mbar_arrive_expect_tx(BAR(kBarKVFull + slot), (uint32_t)nbox * p.box_rows * 128u * 2u);
-                for (int k = 0; k < boxes; ++k) {
-                    if (slot0[k] < 0)
-                        continue;
-                    const uint32_t roff = (uint32_t)k * p.box_rows * 128u;
-                    tma_load_3d(dst + roff, map, 0, kvh, slot0[k], BAR(kBarKVFull + slot));
-                    tma_load_3d(dst + kKVHalf + roff, map, 64, kvh, slot0[k], BAR(kBarKVFull + slot));
-                }
+                __syncwarp();
             }
         }
-        __syncwarp();
-    } else if (warp >= 9) {
-        // ================== MMA issuer for query tile i = warp - 9 ==================
+    } else if (warp == 9) {
+        // ============================ MMA issuer ============================
+        // One lane issues for both query tiles in the fixed order S_0(n), S_1(n), PV_0(n),
+        // PV_1(n).  S_i(n) overwrites the TMEM columns P_i(n-1) occupied, so it is issued only
+        // after PV_i(n-1) has completed; in this order another group of MMAs always sits between
+        // the two, so the tensor pipe does not drain while the issuer waits, and each tile's
+        // softmax runs while the tensor core works for the other tile.
         constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);   // Q, K both K-major
-        constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kD, false, true);     // P K-major, V MN-major
-        const int i = warp - 9;
-        const int my_nkv = nkv[i];
-        const uint32_t qtile = base + kOffQ + i * kQTile;
-        const uint32_t o_tmem = tmem + 256 + i * 128;
-        bool ok = my_nkv == 0 || __all_sync(0xffffffffu, mbar_wait(BAR(kBarQ), 0));
-        auto issue_s = [&](int n) {
+        constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kD, false, true);     // P (TMEM), V MN-major
+        bool ok = __all_sync(0xffffffffu, mbar_wait(BAR(kBarQ), 0));
+        auto wait_all = [&](uint32_t b_, uint32_t parity) {
+            ok = ok && __all_sync(0xffffffffu, mbar_wait(b_, parity));
+            return ok;
+        };
+        auto issue_s = [&](int i, int n) {
             const int t = 2 * n;
             const int slot = t % kSlots;
-            const int bb = n & 1;
-            ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarKVFull + slot), (t / kSlots) & 1));
-            if (n >= 2)
-                ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarSFree + 2 * i + bb), ((n - 2) >> 1) & 1));
-            if (!ok)
+            if (!wait_all(BAR(kBarKVFull + slot), (t / kSlots) & 1))
+                return;
+            if (n >= 1 && !wait_all(BAR(kBarODone + i), (n - 1) & 1))
                 return;
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t ktile = base + kOffKV + slot * kKVTile;
-                const uint32_t s_tmem = tmem + i * 128 + bb * 64;
+                const uint32_t qtile = base + kOffQ + i * kTile;
+                const uint32_t ktile = base + kOffKV + slot * kTile;
 #pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk)
-                    mma_bf16_ss(s_tmem, smem_desc_sw128(qtile + (kk >> 2) * kQHalf + (kk & 3) * 32, 16, 1024),
-                                smem_desc_sw128(ktile + (kk >> 2) * kKVHalf + (kk & 3) * 32, 16, 1024), idesc_s,
-                                kk > 0 ? 1u : 0u);
-                mma_commit(BAR(kBarSFull + 2 * i + bb));
-                mma_commit(BAR(kBarKVEmpty + slot));
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + i * 256, smem_desc_sw128(qtile + off, 16, 1024),
+                                smem_desc_sw128(ktile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(BAR(kBarSFull + i));
+                // the last use of K(n) (S_1(n), or S_0(n) when tile 1 is done): release its slot
+                if (i == 1 || n >= nkv[1])
+                    mma_commit(BAR(kBarKVEmpty + slot));
             }
             __syncwarp();
         };
-        auto issue_pv = [&](int m) {
-            const int t = 2 * m + 1;
+        auto issue_pv = [&](int i, int n) {
+            const int t = 2 * n + 1;
             const int slot = t % kSlots;
-            const int bb = m & 1;
-            ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarKVFull + slot), (t / kSlots) & 1));
-            if (!ok)
+            if (!wait_all(BAR(kBarKVFull + slot), (t / kSlots) & 1))
                 return;
-            const uint32_t vtile = base + kOffKV + slot * kKVTile;
-            const int vrows = kv_len - m * kBN;
-            if (vrows < kBN) {
+            const uint32_t vtile = base + kOffKV + slot * kTile;
+            const int vrows = kv_len - n * kBN;
+            const bool first_use = (i == 0) || n >= nkv[0];     // PV_0(n) precedes PV_1(n)
+            if (vrows < kBN && first_use) {
                 // Keys past the sequence carry P = 0, but their V rows may hold anything (NaN
-                // patterns included) and 0 * NaN would poison O: zero them.  Both issuers may
-                // do this for the last tile; they write the same zeros.
+                // patterns included) and 0 * NaN would poison O: zero them.
                 const int per_half = (kBN - vrows) * 8;        // 16-byte chunks
                 for (int c = lane; c < 2 * per_half; c += 32) {
                     const int half = c / per_half;
                     const int rem = c % per_half;
-                    sts_u4(vtile + half * kKVHalf + (uint32_t)(vrows + rem / 8) * 128u + (uint32_t)(rem % 8) * 16u,
+                    sts_u4(vtile + half * kHalf + (uint32_t)(vrows + rem / 8) * 128u + (uint32_t)(rem % 8) * 16u,
                            make_uint4(0, 0, 0, 0));
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            ok = ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarPFull + 2 * i + bb), (m >> 1) & 1));
-            if (!ok)
+            if (!wait_all(BAR(kBarPFull + i), n & 1))
                 return;
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t ptile = base + kOffP + (2 * i + bb) * kPTile;
+                const uint32_t s_tmem = tmem + i * 256;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_bf16_ss(o_tmem, smem_desc_sw128(ptile + kk * 32, 16, 1024),
-                                smem_desc_sw128(vtile + kk * 16 * 128, kKVHalf, 1024), idesc_o,
-                                (m > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(BAR(kBarODone + 2 * i + bb));
-                mma_commit(BAR(kBarKVEmpty + slot));
+                    mma_bf16_ts(s_tmem + 128, s_tmem + kk * 8, smem_desc_sw128(vtile + kk * 16 * 128, kHalf, 1024),
+                                idesc_o, (n > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(BAR(kBarODone + i));
+                // the last use of V(n) (PV_1(n), or PV_0(n) when tile 1 is done): release its slot
+                if (i == 1 || n >= nkv[1])
+                    mma_commit(BAR(kBarKVEmpty + slot));
             }
             __syncwarp();
         };
-        if (my_nkv > 0)
-            issue_s(0);
-        for (int n = 0; n < my_nkv && ok; ++n) {
-            if (n + 1 < my_nkv)
-                issue_s(n + 1);      // the next scores are computed while this tile's softmax runs
-            issue_pv(n);
-        }
-        // Key tiles this query tile never needs still count toward their slot's release: wait
-        // until the tile is loaded (so the arrival lands in the right phase), then arrive.
-        for (int t = 2 * my_nkv; t < 2 * nkv_all && ok; ++t) {
-            const int slot = t % kSlots;
-            ok = __all_sync(0xffffffffu, mbar_wait(BAR(kBarKVFull + slot), (t / kSlots) & 1));
-            if (ok && lane == 0)
-                mbar_arrive(BAR(kBarKVEmpty + slot));
-            __syncwarp();
+        for (int n = 0; n < nkv_all && ok; ++n) {
+            if (n < nkv[0])
+                issue_s(0, n);
+            if (n < nkv[1])
+                issue_s(1, n);
+            if (n < nkv[0])
+                issue_pv(0, n);
+            if (n < nkv[1])
+                issue_pv(1, n);
         }
         if (!ok && lane == 0)
             flag_error(p.d_err, NV_DERR_TIMEOUT);
@@ -336,109 +423,76 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = warp >> 2;
         const int r = threadIdx.x & 127;                // tile row == TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t s_col = tmem + lane_base + i * 128;
-        const uint32_t o_addr = tmem + lane_base + 256 + i * 128;
-        const int tok = i0[i] + (r >> p.group_shift);   // token index inside the chunk
+        const uint32_t s_addr = tmem + lane_base + i * 256;
+        const uint32_t o_addr = s_addr + 128;
+        const int my_i0 = i ? i0[1] : i0[0];
+        const int my_first_masked = i ? first_masked[1] : first_masked[0];
+        const int n_end = i ? nkv[1] : nkv[0];
+        const int tok = my_i0 + (r >> p.group_shift);   // token index inside the chunk
         const int head = (int)kvh * p.group + (r & (p.group - 1));
         const bool valid = tok < Lq;
         const int lim = P + tok;                        // last key this row may see
         float m_run = -INFINITY;                        // running max of scale*log2(e)*s
         float l_run = 0.f;
         bool ok = true;
-        const int n_end = nkv[i];
         for (int n = 0; n < n_end && ok; ++n) {
-            const int bb = n & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(BAR(kBarSFull + 2 * i + bb), (n >> 1) & 1))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(kBarSFull + i), n & 1))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t sv[64];
-            tmem_ld32x2(s_col + bb * 64, sv);
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(BAR(kBarSFree + 2 * i + bb));
+            const bool masked = n >= my_first_masked;
+            const int rel = lim - n * kBN;              // keys j <= rel of this tile are visible
+            uint32_t pk[64];
             float s[64];
-#pragma unroll
-            for (int j = 0; j < 64; ++j)
-                s[j] = __uint_as_float(sv[j]);
-            if (n >= first_masked[i]) {
-                const int rel = lim - n * kBN;          // keys j <= rel are visible
-#pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    s[j] = (j <= rel) ? s[j] : -INFINITY;
-            }
-            // row max: a tree, so the compare chain is 6 deep instead of 64
-            float mx8[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                mx8[j] = fmaxf(fmaxf(fmaxf(s[j], s[j + 8]), fmaxf(s[j + 16], s[j + 24])),
-                               fmaxf(fmaxf(s[j + 32], s[j + 40]), fmaxf(s[j + 48], s[j + 56])));
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+            // exponentials against the running max, two halves of 64 keys
+            const float neg_m0 = (m_run == -INFINITY) ? 0.f : -m_run;
+            load_scores(s_addr, masked, rel, s);
+            float mx = max64(s);
+            float rs = exp_pack64(s, p.scale_log2, neg_m0, pk);
+            load_scores(s_addr + 64, masked, rel - 64, s);
+            mx = fmaxf(mx, max64(s));
+            rs += exp_pack64(s, p.scale_log2, neg_m0, pk + 32);
             const float mx2 = mx * p.scale_log2;
             const bool need = mx2 > m_run + kRescaleLog2;
-            const float m_new = need ? mx2 : m_run;
-            const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;   // m_run = -inf -> 0
-            const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
-            uint32_t pk[32];
-            float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            float alpha = 1.f;
+            if (__any_sync(0xffffffffu, need)) {
+                // the max moved (first tile, or rarely later): redo the row with the new max
+                if (need) {
+                    alpha = fast_exp2(m_run - mx2);     // m_run = -inf -> 0
+                    m_run = mx2;
+                }
+                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+                load_scores(s_addr, masked, rel, s);
+                rs = exp_pack64(s, p.scale_log2, neg_m, pk);
+                load_scores(s_addr + 64, masked, rel - 64, s);
+                rs += exp_pack64(s, p.scale_log2, neg_m, pk + 32);
+                if (n >= 1) {
+                    // O_i holds PV_i(0..n-1), all complete: S_i(n) was issued after PV_i(n-1) finished
 #pragma unroll
-            for (int j = 0; j < 64; j += 2) {
-                // every fourth pair on the FMA pipe, the rest on the special-function unit
-                const bool poly = ((j >> 1) & 3) == 3;
-                const float x0 = fmaf(s[j], p.scale_log2, neg_m);
-                const float x1 = fmaf(s[j + 1], p.scale_log2, neg_m);
-                const float p0 = poly ? exp2_poly3(x0) : fast_exp2(x0);
-                const float p1 = poly ? exp2_poly3(x1) : fast_exp2(x1);
-                rs8[(j >> 1) & 7] += p0 + p1;
-                pk[j >> 1] = pack_bf16x2(p0, p1);
+                    for (int c = 0; c < kD / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(o_addr + c * 32, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+                        tmem_st32(o_addr + c * 32, v);
+                    }
+                }
             }
-            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
             l_run = l_run * alpha + rs;
-            m_run = m_new;
-            // P buffer bb is free once PV_i(n-2) has completed
-            if (n >= 2 && !__all_sync(0xffffffffu, mbar_wait(BAR(kBarODone + 2 * i + bb), ((n - 2) >> 1) & 1))) {
-                ok = false;
-                break;
-            }
-            const uint32_t ptile = base + kOffP + (2 * i + bb) * kPTile;
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                sts_u4(ptile + sw128((uint32_t)r, (uint32_t)c),
-                       make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]));
-            // rare: rescale this row's O (PV_i(n-1) must be complete first; nothing to do at n = 0)
-            if (n >= 1 && __any_sync(0xffffffffu, need)) {
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(BAR(kBarODone + 2 * i + ((n - 1) & 1)), ((n - 1) >> 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < kD / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(o_addr + c * 32, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-                    tmem_st32(o_addr + c * 32, v);
-                }
-                tmem_wait_st();
-            }
-            fence_proxy_async_smem();
+            // P_i(n) as bf16 pairs over the first 64 columns of S_i (A operand of the PV MMA)
+            tmem_st64(s_addr, pk);
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(BAR(kBarPFull + 2 * i + bb));
+                mbar_arrive(BAR(kBarPFull + i));
         }
         // ---- epilogue: O / l -> bf16 rows ----
         if (n_end > 0) {
-            const int last = n_end - 1;
-            if (ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarODone + 2 * i + (last & 1)), (last >> 1) & 1))) {
+            if (ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarODone + i), (n_end - 1) & 1))) {
                 tc_fence_after();
                 const float inv = (valid && l_run > 0.f) ? 1.f / l_run : 0.f;
                 uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(cq0 + tok) * p.num_q_heads + head) * kD);
