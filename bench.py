@@ -100,6 +100,26 @@ def profiled_traffic(kernel_key: str, sources) -> float | None:
     return float(e["dram_bytes_per_launch"])
 
 
+def reduce_over_ranks(x: float, op: str, world: int, device="cpu") -> float:
+    """Max or sum of a host scalar over the ranks of the default process group (identity at 1 rank)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_decode_batch(rank: int, num_seqs: int = 512) -> W.PagedBatch:
+    """Each rank's own Qwen3-8B-shaped decode batch (weak scaling: same shape, different seed)."""
+    return W.qwen8_decode(seed=rank, num_seqs=num_seqs)
+
+
+def rank_prefill_batch(rank: int) -> W.PagedBatch:
+    return W.prefill_chunk(seed=rank)
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
 
@@ -183,24 +203,18 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize()
 
+    red_dev = dev if (world > 1 and dist.get_backend() == "nccl") else "cpu"
+
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_over_ranks(x, "max", world, red_dev)
 
     def sum_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev if dist.get_backend() == "nccl" else "cpu")
-        dist.all_reduce(t, op=dist.ReduceOp.SUM)
-        return float(t.item())
+        return reduce_over_ranks(x, "sum", world, red_dev)
 
     pk, pk_kind = peaks()
 
     # ---------------- decode phase: store + decode on the Qwen3-8B batch ----------------
-    db = W.qwen8_decode(seed=rank)
+    db = rank_decode_batch(rank)
     kc, vc = db.cache()
     k_cache, v_cache = to_dev(kc), to_dev(vc)
     del kc, vc
@@ -277,7 +291,7 @@ def run_ours(args, rank, world, local_rank):
         # ---------------- prefill phase: store + prefill on the chunked-prefill batch ----------------
         del k_cache, v_cache, ws
         torch.cuda.empty_cache()
-        pb = W.prefill_chunk(seed=rank)
+        pb = rank_prefill_batch(rank)
         pkc, pvc = pb.cache()
         pk_cache, pv_cache = to_dev(pkc), to_dev(pvc)
         del pkc, pvc
