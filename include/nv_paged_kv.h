@@ -125,6 +125,35 @@ int nv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache
                          nv_stream_t stream);
 
 /*
+ * nv_paged_decode_attn_noalloc -- nv_paged_decode_attn without a caller-provided workspace.
+ *
+ * The source pages have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory when they run decode -- an engine whose KV pool already took all the
+ * memory its allocator may hand out, a host application that lends the library only its
+ * tensors, or C code with no CUDA allocator at hand.  It allocates nothing: the split-KV
+ * partials live in a fixed device array of NV_DECODE_STATIC_SCRATCH_BYTES inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ *
+ * Arguments and results are those of nv_paged_decode_attn (same kernels).  The split length
+ * is the usual one, doubled (up to 4096 positions) while the partials would not fit the
+ * array; a batch whose partials still exceed it (num_seqs * splits * num_q_heads * 520 bytes)
+ * is rejected with NV_ERR_WORKSPACE before anything is enqueued.
+ *
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  All calls share the
+ * one array and it keeps the last call's contents (nothing in it needs to start at zero):
+ * calls that overlap on the GPU -- on different streams, or from different threads -- race on
+ * it and give wrong results.  Serialise them.
+ */
+#define NV_DECODE_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                 const int32_t *block_tables, int32_t bt_stride, const int32_t *context_lens,
+                                 int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
+                                 void *out, int32_t *d_err, nv_stream_t stream);
+
+/*
  * nv_paged_prefill_attn -- varlen causal prefill over a cached prefix plus the new chunk.
  *
  * Field guide Step 10.3 (prefill branch, prefix cache) and Step 07.5: the new tokens of all

@@ -29,7 +29,7 @@ NV_DERR_LENGTH = 0x4
 NV_DERR_TIMEOUT = 0x8
 
 EXPORTED = ("nv_status_string", "nv_store_kvcache", "nv_paged_decode_workspace_size", "nv_paged_decode_attn",
-            "nv_paged_prefill_attn")
+            "nv_paged_decode_attn_noalloc", "nv_paged_prefill_attn")
 
 
 class NvError(RuntimeError):
@@ -63,6 +63,8 @@ def load_library(path: str | None = None):
     L.nv_paged_decode_workspace_size.restype = sz
     L.nv_paged_decode_attn.argtypes = [V, V, V, V, i32, V, i32, i32, i32, i32, i32, i32, i32, f32, V, V, sz, V, V]
     L.nv_paged_decode_attn.restype = ctypes.c_int
+    L.nv_paged_decode_attn_noalloc.argtypes = [V, V, V, V, i32, V, i32, i32, i32, i32, i32, i32, i32, f32, V, V, V]
+    L.nv_paged_decode_attn_noalloc.restype = ctypes.c_int
     L.nv_paged_prefill_attn.argtypes = [V, V, V, V, V, V, i32, i32, i32, i32, i32, i32, i32, i32, i32, f32, V, V, V]
     L.nv_paged_prefill_attn.restype = ctypes.c_int
     if path is None:
@@ -142,6 +144,28 @@ def nv_paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale,
         hkv, d, bs, nb, int(max_context_len), float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_err),
         _stream(stream))
     _check("nv_paged_decode_attn", rc)
+    return out
+
+
+def nv_paged_decode_attn_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
+                                 max_context_len=None, d_err=None, stream=None):
+    """``nv_paged_decode_attn`` for callers that cannot allocate device memory: no workspace, the
+    split-KV partials live in a fixed array inside the library (see the C header for the limit).
+    Calls sharing that array must not overlap on the GPU.  ``out`` must be given to allocate nothing."""
+    import torch
+    nb, bs, hkv, d = _pool_shape(k_cache, v_cache)
+    B, hq, dq = (int(x) for x in q.shape)
+    _need(dq == d and q.is_contiguous(), "q must be contiguous [B, Hq, D]")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == B and block_tables.stride(1) == 1,
+          "block_tables must be [B, W] with unit column stride")
+    if max_context_len is None:
+        max_context_len = int(block_tables.shape[1]) * bs
+    if out is None:
+        out = torch.empty_like(q)
+    rc = load_library().nv_paged_decode_attn_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.stride(0), _ptr(context_lens), B, hq,
+        hkv, d, bs, nb, int(max_context_len), float(scale), _ptr(out), _ptr(d_err), _stream(stream))
+    _check("nv_paged_decode_attn_noalloc", rc)
     return out
 
 

@@ -24,6 +24,8 @@
 //   * A sequence split over several CTAs writes unnormalised partial outputs plus its
 //     (max, sum); a small merge kernel combines them.  Single-split sequences write bf16
 //     output directly.
+#include <mutex>
+
 #include "nv_common.cuh"
 
 namespace {
@@ -503,6 +505,122 @@ extern "C" int nv_paged_decode_attn(const void *q, const void *k_cache, const vo
         if (!workspace || workspace_bytes < need || !aligned16(workspace))
             return NV_ERR_WORKSPACE;
         p.part_o = static_cast<float *>(workspace);
+        p.part_ml = p.part_o + (size_t)num_seqs * p.max_splits * num_q_heads * kD;
+    }
+    const size_t smem = (size_t)kStages * 2 * kT * num_kv_heads * kD * 2 + 2 * kStages * 8 + kStages * 4 + 16;
+    if (num_kv_heads <= 8)
+        return dispatch_group<8>(group, p, num_seqs, smem, (cudaStream_t)stream);
+    return dispatch_group<16>(group, p, num_seqs, smem, (cudaStream_t)stream);
+}
+
+// ---------------------------------------------------------------------------------------
+// Allocation-free decode.
+//
+// Some callers cannot allocate device memory at the point where they run decode: an engine
+// whose KV pool was sized to take all the memory its allocator may use, a host application
+// that only lends the library its tensors (the library sees raw pointers and has no
+// allocator of its own), or C code with no CUDA allocator at hand.  For them the split-KV
+// partials live in a fixed array below, which every GPU that loads this library holds until
+// the process exits.
+// ---------------------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_decode_scratch[NV_DECODE_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of g_decode_scratch on the current device.  Looked up once per device (the
+// host-side name is only a stand-in for the device array, never an address to pass a kernel).
+void *static_scratch(int *status)
+{
+    static std::mutex mu;
+    static void *addr[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *status = NV_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr) {
+            *status = NV_ERR_CUDA;
+            return nullptr;
+        }
+        addr[dev] = ptr;
+    }
+    return addr[dev];
+}
+
+}  // namespace
+
+extern "C" int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                            const int32_t *block_tables, int32_t bt_stride,
+                                            const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                            int32_t num_blocks, int32_t max_context_len, float scale, void *out,
+                                            int32_t *d_err, nv_stream_t stream)
+{
+    using namespace nvkv_host;
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || bt_stride <= 0 || num_blocks < 0 ||
+        max_context_len < 0)
+        return NV_ERR_SHAPE;
+    if (num_seqs == 0)
+        return NV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return NV_ERR_NULL;
+    if (head_dim != kD)
+        return NV_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads != 0)
+        return NV_ERR_SHAPE;
+    const int group = num_q_heads / num_kv_heads;
+    if (num_kv_heads > 16 || (group != 1 && group != 2 && group != 4 && group != 8))
+        return NV_ERR_UNSUPPORTED;
+    if (!is_pow2(block_size) || block_size < 16 || block_size > 256)
+        return NV_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return NV_ERR_ALIGN;
+    if ((int64_t)num_blocks * block_size * num_kv_heads * kD >= (1ll << 40))
+        return NV_ERR_UNSUPPORTED;
+    if (max_context_len == 0)
+        max_context_len = 1;
+    const int64_t bt_cap = (int64_t)bt_stride * block_size;
+    const int max_len = (int)(bt_cap < max_context_len ? bt_cap : max_context_len);
+
+    // The usual split length, doubled until the partials fit in the static array.
+    int split = decode_split_tokens(num_seqs, max_context_len);
+    auto need = [&](int sp) {
+        const int splits = (max_len + sp - 1) / sp;
+        return splits <= 1 ? (size_t)0 : (size_t)num_seqs * splits * num_q_heads * (kD + 2) * sizeof(float);
+    };
+    while (need(split) > (size_t)NV_DECODE_STATIC_SCRATCH_BYTES && split < 4096)
+        split *= 2;
+    if (need(split) > (size_t)NV_DECODE_STATIC_SCRATCH_BYTES)
+        return NV_ERR_WORKSPACE;   // partials of this batch exceed the static array
+
+    DecodeParams p{};
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.k_cache = static_cast<const __nv_bfloat16 *>(k_cache);
+    p.v_cache = static_cast<const __nv_bfloat16 *>(v_cache);
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.d_err = d_err;
+    p.bt_stride = bt_stride;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.block_shift = ilog2(block_size);
+    p.num_blocks = num_blocks;
+    p.max_len = max_len;
+    p.split_tokens = split;
+    p.max_splits = (max_len + split - 1) / split;
+    p.scale_log2 = scale * nvkv::kLog2e;
+    if (p.max_splits > 1) {
+        int status = NV_OK;
+        void *scratch = static_scratch(&status);
+        if (!scratch)
+            return status;
+        // Every partial the merge reads is written earlier in the same call, so nothing in the
+        // array has to start at zero.
+        p.part_o = static_cast<float *>(scratch);
         p.part_ml = p.part_o + (size_t)num_seqs * p.max_splits * num_q_heads * kD;
     }
     const size_t smem = (size_t)kStages * 2 * kT * num_kv_heads * kD * 2 + 2 * kStages * 8 + kStages * 4 + 16;

@@ -1,0 +1,67 @@
+"""The allocation-free decode entry point, called through the C ABI, against the allocating one.
+
+Some callers cannot allocate device memory when they run decode: an engine whose KV pool already
+took all the memory its allocator may hand out, a host application that lends the library only
+its tensors, or C code with no CUDA allocator at hand.  nv_paged_decode_attn_noalloc serves them:
+its split-KV partials live in a fixed device array inside the library.  Two calls in a row must
+each match nv_paged_decode_attn (the array keeps the previous call's contents, and nothing may
+depend on them).  This file is collected last, so a run that stops at the first failure has run
+every other test before it."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import workloads as W
+from tests.gpu_util import DeviceBatch, compare, host_f32
+
+pytestmark = pytest.mark.gpu
+
+V, I32, F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+NV_ERR_WORKSPACE = -5
+
+
+def _c_entry():
+    import paged_kv_attention_store_gb300 as nv
+    f = nv.load_library().nv_paged_decode_attn_noalloc
+    f.argtypes = [V, V, V, V, I32, V, I32, I32, I32, I32, I32, I32, I32, F32, V, V, V]
+    f.restype = ctypes.c_int
+    return f
+
+
+def _call(f, db, out, max_ctx):
+    import torch
+    b = db.b
+    nb, bs, hkv, d = (int(x) for x in db.k_cache.shape)
+    return f(db.q.data_ptr(), db.k_cache.data_ptr(), db.v_cache.data_ptr(), db.block_tables.data_ptr(),
+             db.block_tables.stride(0), db.seq_lens.data_ptr(), b.num_seqs, b.num_q_heads, hkv, d, bs, nb,
+             max_ctx, b.scale, out.data_ptr(), db.d_err.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.mark.parametrize("make", [W.qwen06_decode, W.qwen8_decode], ids=["qwen3-0.6b", "qwen3-8b"])
+def test_noalloc_matches_allocating_entry_point_twice(make):
+    import torch
+    b = make()
+    db = DeviceBatch(b)
+    db.store()
+    max_ctx = int(b.seq_lens.max())
+    want = host_f32(db.decode(max_context_len=max_ctx))           # the allocating entry point
+    assert db.err() == 0
+    f = _c_entry()
+    for call in range(2):
+        out = torch.full_like(db.q, float("nan"))
+        assert _call(f, db, out, max_ctx) == 0
+        got = host_f32(out)
+        assert db.err() == 0
+        rows = b.seq_lens > 0
+        compare(got[rows], want[rows], f"noalloc call {call}")
+        assert not got[~rows].any()
+
+
+def test_noalloc_rejects_a_batch_beyond_the_static_array():
+    """1024 sequences x 64 heads x 8192 positions need more partials than the array holds even at the
+    longest split: rejected on the host, nothing enqueued (the pointers are never touched)."""
+    f = _c_entry()
+    fake = 0x10000
+    rc = f(fake, fake, fake, fake, 32, fake, 1024, 64, 8, 128, 256, 64, 8192, 0.088, fake, None, None)
+    assert rc == NV_ERR_WORKSPACE
