@@ -5,30 +5,31 @@
 // and Lk = cu_k[b+1]-cu_k[b] keys read through its block table; the first P = Lk-Lq were
 // cached before.  Query i of the chunk sees keys 0..P+i (bottom-right causal alignment).
 //
-// How (GB300 design; the pages call a library kernel here).  One CTA computes TWO 128-row
-// query tiles of one (sequence, kv head).  With G = Hq/Hkv query heads per kv head a tile
-// packs 128/G consecutive tokens x G heads, so every K/V tile loaded serves 256 query rows.
-// Key tiles are 128 keys: on GB300 an M=128 tcgen05.mma costs about the same ~96 cycles for
-// N=64 as for N=128, so narrower tiles leave most of the tensor core idle.
-//   * warp 8 (TMA producer): both Q tiles with one 3-D tensor-map copy per 64-dim half
-//     (dims head_dim, q head, token), then K and V tiles (128 keys x 128 dims) straight from
-//     the paged pool (dims head_dim, kv head, slot), 128-byte swizzled, into a 5-slot ring
+// How (GB300 design; the pages call a library kernel here).  One CTA computes one 128-row
+// query tile of one (sequence, kv head); with G = Hq/Hkv query heads per kv head the tile packs
+// 128/G consecutive tokens x G heads, so every K/V tile loaded serves all G heads.
+//   * warp 4 (TMA producer): the Q tile with one 3-D tensor-map copy per 64-dim half (dims
+//     head_dim, q head, token), then K and V tiles of 128 keys x 128 dims straight from the
+//     paged pool (dims head_dim, kv head, slot), 128-byte swizzled, into a 6-slot ring
 //     K0 V0 K1 V1 ...; the sequence's block-table row is held 32 entries at a time in the
 //     warp's registers, so a copy never waits on a dependent table load.
-//   * warp 9 (MMA issuer; owns the TMEM allocation): one lane issues tcgen05.mma kind::f16
-//     with fp32 accumulators in tensor memory: S_i(n) = Q_i K(n)^T (both operands from
-//     shared memory) and O_i += P_i(n) V(n) with P_i read from TENSOR memory, where the
-//     softmax wrote it over S_i.  The issue order S_0(n), S_1(n), PV_0(n), PV_1(n) makes the
-//     two tiles alternate: one tile's products run on the tensor core while the other tile's
-//     softmax runs.  (Issued independently, the tiles fall into lockstep, and the tensor core
-//     and the exp unit each sit idle half the time.)
-//   * warps 0-3 / 4-7 (softmax warpgroups, one per query tile): thread r owns row r = TMEM
-//     lane r.  It reads its 128 scores in two 64-column halves, computes the exponentials
-//     against the running max while the tile max forms (a row is redone only when the max
-//     moves past the lazy-rescale threshold of 2^8, i.e. almost only on the first tile),
-//     masks only on tiles that cross the diagonal, writes P as bf16 pairs back into the S
-//     columns (tcgen05.st), rescales O in TMEM in the rare moved-max case, and at the end
+//   * warp 5 (MMA issuer; owns the TMEM allocation): one lane issues tcgen05.mma kind::f16
+//     with fp32 accumulators in tensor memory.  TMEM holds THREE score buffers of 128 columns
+//     and the 128-column O accumulator.  S(n) = Q K(n)^T (operands in shared memory) goes to
+//     buffer n % 3; the softmax writes P(n) as bf16 pairs over the first half of that buffer;
+//     O += P(n) V(n) reads P from tensor memory.  S(n+2) is issued right after PV(n): its
+//     buffer last held P(n-1), whose PV finished an iteration earlier, so the issuer never
+//     waits on a group it has just queued and the tensor pipe stays fed while the softmax of
+//     tile n+1 runs.  (Sharing one score buffer with P forces S(n+1) to wait for PV(n) to
+//     complete, which drains the pipe every iteration.)
+//   * warps 0-3 (softmax / correction / epilogue): thread r owns row r = TMEM lane r.  It loads
+//     its 128 scores at once, masks only on tiles that cross the diagonal, keeps a base-2 online
+//     softmax with a lazy rescale (the running max moves only when a score beats it by more
+//     than 8; only then is O rescaled in TMEM), writes P with tcgen05.st, and at the end
 //     normalises O and stores bf16 rows.
+// Tile shapes follow measurements on GB300: an M=128 tcgen05.mma costs about the same for N=64
+// as for N=128, so key tiles are 128 wide; a group of 8 MMAs queued behind others streams at
+// ~800 cycles but costs ~1100 issued into an empty pipe.
 // Every mbarrier wait is bounded; on timeout the kernel records NV_DERR_TIMEOUT and stops.
 #include <cuda.h>
 
@@ -43,9 +44,11 @@ using namespace nvkv;
 constexpr int kD = 128;
 constexpr int kBM = 128;             // rows per query tile (TMEM lanes)
 constexpr int kBN = 128;             // keys per K/V tile
-constexpr int kSlots = 5;            // K/V ring slots
-constexpr int kThreads = 320;        // warps 0-3, 4-7 softmax; 8 producer; 9 MMA
-constexpr uint32_t kTmemCols = 512;  // tile i: S_i / P_i at i*256 + [0, 128), O_i at i*256 + [128, 256)
+constexpr int kSlots = 6;            // K/V ring slots
+constexpr int kBufs = 3;             // score / P buffers in TMEM
+constexpr int kThreads = 192;        // warps 0-3 softmax; 4 producer; 5 MMA
+constexpr uint32_t kTmemCols = 512;  // buffer b at b*128, O at 384
+constexpr uint32_t kTmemO = 384;
 constexpr float kRescaleLog2 = 8.0f;
 // Of every 8 score pairs, this many take the polynomial exp2 on the FMA pipe; the rest use the
 // special-function unit.
@@ -56,16 +59,16 @@ constexpr int kPolyPairs = NVKV_PREFILL_POLY_PAIRS;
 
 constexpr uint32_t kHalf = 128 * 128;         // 128 rows x 64 dims bf16 (one swizzle atom wide) = 16 KB
 constexpr uint32_t kTile = 2 * kHalf;         // a 128 x 128 bf16 operand = 32 KB
-constexpr uint32_t kOffQ = 0;                 // Q[i] at i*kTile
-constexpr uint32_t kOffKV = 2 * kTile;        // slot s at s*kTile
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffKV = kTile;            // slot s at kOffKV + s*kTile
 constexpr uint32_t kOffBar = kOffKV + kSlots * kTile;
 constexpr int kBarQ = 0;
 constexpr int kBarKVFull = 1;                      // + slot
 constexpr int kBarKVEmpty = kBarKVFull + kSlots;   // + slot
-constexpr int kBarSFull = kBarKVEmpty + kSlots;    // + i
-constexpr int kBarPFull = kBarSFull + 2;           // + i
-constexpr int kBarODone = kBarPFull + 2;           // + i
-constexpr int kNumBars = kBarODone + 2;
+constexpr int kBarSFull = kBarKVEmpty + kSlots;    // + buffer
+constexpr int kBarPFull = kBarSFull + kBufs;       // + buffer
+constexpr int kBarODone = kBarPFull + kBufs;       // + buffer (PV(n) commits to n % 3)
+constexpr int kNumBars = kBarODone + kBufs;
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffTmemSlot + 16 + 1024;      // + slack for 1024-byte alignment
 
@@ -82,7 +85,7 @@ struct PrefillParams {
     int32_t block_shift;    // log2 block_size
     int32_t box_rows;       // min(block_size, kBN)
     int32_t num_blocks;
-    int32_t max_pairs;      // gridDim.z
+    int32_t max_tiles;      // gridDim.z
     float scale_log2;
 };
 
@@ -218,22 +221,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
     const int tq = kBM >> p.group_shift;                   // query tokens per tile
-    const int npairs = (Lq + 2 * tq - 1) / (2 * tq);
-    if (npairs > p.max_pairs && blockIdx.z == 0 && kvh == 0 && threadIdx.x == 0)
+    const int ntiles = (Lq + tq - 1) / tq;
+    if (ntiles > p.max_tiles && blockIdx.z == 0 && kvh == 0 && threadIdx.x == 0)
         flag_error(p.d_err, NV_DERR_LENGTH);
-    const int pair = p.max_pairs - 1 - (int)blockIdx.z;    // the heaviest pairs are dispatched first
-    if (pair >= npairs)
+    const int tile = p.max_tiles - 1 - (int)blockIdx.z;    // the heaviest tiles are dispatched first
+    if (tile >= ntiles)
         return;
-    int i0[2], nq[2], nkv[2], first_masked[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        i0[i] = pair * 2 * tq + i * tq;
-        nq[i] = max(0, min(tq, Lq - i0[i]));
-        nkv[i] = nq[i] > 0 ? (P + i0[i] + nq[i] + kBN - 1) / kBN : 0;
-        first_masked[i] = (P + i0[i] + 1) / kBN;           // key tiles before this need no mask
-    }
-    const int kv_len = P + i0[nq[1] > 0 ? 1 : 0] + nq[nq[1] > 0 ? 1 : 0];   // keys any row can see
-    const int nkv_all = max(nkv[0], nkv[1]);
+    const int i0 = tile * tq;
+    const int nq = min(tq, Lq - i0);
+    const int kv_len = P + i0 + nq;                        // keys any row of the tile can see
+    const int nkv = (kv_len + kBN - 1) / kBN;
+    const int first_masked = (P + i0 + 1) / kBN;           // key tiles before this need no mask
 
     const uint32_t bar = base + kOffBar;
     auto BAR = [&](int i) { return bar + 8u * (uint32_t)i; };
@@ -245,14 +243,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(kBarKVFull + s), 1);
             mbar_init(BAR(kBarKVEmpty + s), 1);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kBufs; ++s) {
             mbar_init(BAR(kBarSFull + s), 1);
             mbar_init(BAR(kBarPFull + s), 4);
             mbar_init(BAR(kBarODone + s), 1);
         }
         fence_barrier_init();
     }
-    if (warp == 9) {
+    if (warp == 5) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -261,20 +259,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 8) {
+    if (warp == 4) {
         // =========================== TMA producer ===========================
         if (lane == 0) {
             prefetch_tmap(&tmap_q);
             prefetch_tmap(&tmap_k);
             prefetch_tmap(&tmap_v);
-            mbar_arrive_expect_tx(BAR(kBarQ), (nq[1] > 0 ? 2u : 1u) * kTile);
-            for (int i = 0; i < 2; ++i) {
-                if (nq[i] == 0)
-                    continue;
-                for (int h = 0; h < 2; ++h)
-                    tma_load_3d(base + kOffQ + i * kTile + h * kHalf, &tmap_q, h * 64, kvh * p.group, cq0 + i0[i],
-                                BAR(kBarQ));
-            }
+            mbar_arrive_expect_tx(BAR(kBarQ), kTile);
+            for (int h = 0; h < 2; ++h)
+                tma_load_3d(base + kOffQ + h * kHalf, &tmap_q, h * 64, kvh * p.group, cq0 + i0, BAR(kBarQ));
         }
         const int32_t *bt = p.block_tables + (size_t)b * p.bt_stride;
         const int nblk = (kv_len + (1 << p.block_shift) - 1) >> p.block_shift;   // entries this CTA reads
@@ -283,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int win_base = 0;
         int win = lane < nblk ? __ldg(bt + lane) : -1;
         bool ok = true;
-        for (int n = 0; n < nkv_all && ok; ++n) {
+        for (int n = 0; n < nkv && ok; ++n) {
             int slot0[kBN / 16];                    // first slot of each box; -1 = skip the box
             int nbox = 0;
             for (int k = 0; k < boxes; ++k) {
@@ -331,13 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == 5) {
         // ============================ MMA issuer ============================
-        // One lane issues for both query tiles in the fixed order S_0(n), S_1(n), PV_0(n),
-        // PV_1(n).  S_i(n) overwrites the TMEM columns P_i(n-1) occupied, so it is issued only
-        // after PV_i(n-1) has completed; in this order another group of MMAs always sits between
-        // the two, so the tensor pipe does not drain while the issuer waits, and each tile's
-        // softmax runs while the tensor core works for the other tile.
         constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);   // Q, K both K-major
         constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kD, false, true);     // P (TMEM), V MN-major
         bool ok = __all_sync(0xffffffffu, mbar_wait(BAR(kBarQ), 0));
@@ -345,39 +333,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = ok && __all_sync(0xffffffffu, mbar_wait(b_, parity));
             return ok;
         };
-        auto issue_s = [&](int i, int n) {
+        auto issue_s = [&](int n) {
             const int t = 2 * n;
             const int slot = t % kSlots;
+            const int bb = n % kBufs;
             if (!wait_all(BAR(kBarKVFull + slot), (t / kSlots) & 1))
                 return;
-            if (n >= 1 && !wait_all(BAR(kBarODone + i), (n - 1) & 1))
+            // buffer bb last held P(n-3): its PV must have finished (one iteration ago)
+            if (n >= kBufs && !wait_all(BAR(kBarODone + bb), ((n - kBufs) / kBufs) & 1))
                 return;
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t qtile = base + kOffQ + i * kTile;
                 const uint32_t ktile = base + kOffKV + slot * kTile;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    mma_bf16_ss(tmem + i * 256, smem_desc_sw128(qtile + off, 16, 1024),
+                    mma_bf16_ss(tmem + bb * 128, smem_desc_sw128(base + kOffQ + off, 16, 1024),
                                 smem_desc_sw128(ktile + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(BAR(kBarSFull + i));
-                // the last use of K(n) (S_1(n), or S_0(n) when tile 1 is done): release its slot
-                if (i == 1 || n >= nkv[1])
-                    mma_commit(BAR(kBarKVEmpty + slot));
+                mma_commit(BAR(kBarSFull + bb));
+                mma_commit(BAR(kBarKVEmpty + slot));
             }
             __syncwarp();
         };
-        auto issue_pv = [&](int i, int n) {
+        auto issue_pv = [&](int n) {
             const int t = 2 * n + 1;
             const int slot = t % kSlots;
+            const int bb = n % kBufs;
             if (!wait_all(BAR(kBarKVFull + slot), (t / kSlots) & 1))
                 return;
             const uint32_t vtile = base + kOffKV + slot * kTile;
             const int vrows = kv_len - n * kBN;
-            const bool first_use = (i == 0) || n >= nkv[0];     // PV_0(n) precedes PV_1(n)
-            if (vrows < kBN && first_use) {
+            if (vrows < kBN) {
                 // Keys past the sequence carry P = 0, but their V rows may hold anything (NaN
                 // patterns included) and 0 * NaN would poison O: zero them.
                 const int per_half = (kBN - vrows) * 8;        // 16-byte chunks
@@ -390,139 +377,125 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            if (!wait_all(BAR(kBarPFull + i), n & 1))
+            if (!wait_all(BAR(kBarPFull + bb), (n / kBufs) & 1))
                 return;
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t s_tmem = tmem + i * 256;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_bf16_ts(s_tmem + 128, s_tmem + kk * 8, smem_desc_sw128(vtile + kk * 16 * 128, kHalf, 1024),
-                                idesc_o, (n > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(BAR(kBarODone + i));
-                // the last use of V(n) (PV_1(n), or PV_0(n) when tile 1 is done): release its slot
-                if (i == 1 || n >= nkv[1])
-                    mma_commit(BAR(kBarKVEmpty + slot));
+                    mma_bf16_ts(tmem + kTmemO, tmem + bb * 128 + kk * 8,
+                                smem_desc_sw128(vtile + kk * 16 * 128, kHalf, 1024), idesc_o,
+                                (n > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(BAR(kBarODone + bb));
+                mma_commit(BAR(kBarKVEmpty + slot));
             }
             __syncwarp();
         };
-        for (int n = 0; n < nkv_all && ok; ++n) {
-            if (n < nkv[0])
-                issue_s(0, n);
-            if (n < nkv[1])
-                issue_s(1, n);
-            if (n < nkv[0])
-                issue_pv(0, n);
-            if (n < nkv[1])
-                issue_pv(1, n);
+        issue_s(0);
+        if (nkv > 1)
+            issue_s(1);
+        for (int n = 0; n < nkv && ok; ++n) {
+            issue_pv(n);
+            if (n + 2 < nkv)
+                issue_s(n + 2);
         }
         if (!ok && lane == 0)
             flag_error(p.d_err, NV_DERR_TIMEOUT);
     } else {
-        // ============ softmax / correction / epilogue: warpgroup i owns query tile i ============
-        const int i = warp >> 2;
-        const int r = threadIdx.x & 127;                // tile row == TMEM lane
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t s_addr = tmem + lane_base + i * 256;
-        const uint32_t o_addr = s_addr + 128;
-        const int my_i0 = i ? i0[1] : i0[0];
-        const int my_first_masked = i ? first_masked[1] : first_masked[0];
-        const int n_end = i ? nkv[1] : nkv[0];
-        const int tok = my_i0 + (r >> p.group_shift);   // token index inside the chunk
+        // ================= softmax / correction / epilogue (warps 0-3) =================
+        const int r = threadIdx.x;                      // tile row == TMEM lane
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const uint32_t o_addr = tmem + lane_base + kTmemO;
+        const int tok = i0 + (r >> p.group_shift);      // token index inside the chunk
         const int head = (int)kvh * p.group + (r & (p.group - 1));
         const bool valid = tok < Lq;
         const int lim = P + tok;                        // last key this row may see
         float m_run = -INFINITY;                        // running max of scale*log2(e)*s
         float l_run = 0.f;
         bool ok = true;
-        for (int n = 0; n < n_end && ok; ++n) {
-            if (!__all_sync(0xffffffffu, mbar_wait(BAR(kBarSFull + i), n & 1))) {
+        for (int n = 0; n < nkv && ok; ++n) {
+            const int bb = n % kBufs;
+            if (!__all_sync(0xffffffffu, mbar_wait(BAR(kBarSFull + bb), (n / kBufs) & 1))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const bool masked = n >= my_first_masked;
+            const uint32_t s_addr = tmem + lane_base + bb * 128;
+            const bool masked = n >= first_masked;
             const int rel = lim - n * kBN;              // keys j <= rel of this tile are visible
-            uint32_t pk[64];
-            float s[64];
-            // exponentials against the running max, two halves of 64 keys
-            const float neg_m0 = (m_run == -INFINITY) ? 0.f : -m_run;
-            load_scores(s_addr, masked, rel, s);
-            float mx = max64(s);
-            float rs = exp_pack64(s, p.scale_log2, neg_m0, pk);
-            load_scores(s_addr + 64, masked, rel - 64, s);
-            mx = fmaxf(mx, max64(s));
-            rs += exp_pack64(s, p.scale_log2, neg_m0, pk + 32);
-            const float mx2 = mx * p.scale_log2;
+            float s0[64], s1[64];
+            load_scores(s_addr, masked, rel, s0);
+            load_scores(s_addr + 64, masked, rel - 64, s1);
+            const float mx2 = fmaxf(max64(s0), max64(s1)) * p.scale_log2;
             const bool need = mx2 > m_run + kRescaleLog2;
             float alpha = 1.f;
-            if (__any_sync(0xffffffffu, need)) {
-                // the max moved (first tile, or rarely later): redo the row with the new max
-                if (need) {
-                    alpha = fast_exp2(m_run - mx2);     // m_run = -inf -> 0
-                    m_run = mx2;
-                }
-                const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-                load_scores(s_addr, masked, rel, s);
-                rs = exp_pack64(s, p.scale_log2, neg_m, pk);
-                load_scores(s_addr + 64, masked, rel - 64, s);
-                rs += exp_pack64(s, p.scale_log2, neg_m, pk + 32);
-                if (n >= 1) {
-                    // O_i holds PV_i(0..n-1), all complete: S_i(n) was issued after PV_i(n-1) finished
-#pragma unroll
-                    for (int c = 0; c < kD / 32; ++c) {
-                        uint32_t v[32];
-                        tmem_ld32(o_addr + c * 32, v);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-                        tmem_st32(o_addr + c * 32, v);
-                    }
-                }
+            if (need) {
+                alpha = fast_exp2(m_run - mx2);         // m_run = -inf -> 0
+                m_run = mx2;
             }
+            const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+            uint32_t pk[64];
+            const float rs = exp_pack64(s0, p.scale_log2, neg_m, pk) + exp_pack64(s1, p.scale_log2, neg_m, pk + 32);
             l_run = l_run * alpha + rs;
-            // P_i(n) as bf16 pairs over the first 64 columns of S_i (A operand of the PV MMA)
-            tmem_st64(s_addr, pk);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(BAR(kBarPFull + i));
-        }
-        // ---- epilogue: O / l -> bf16 rows ----
-        if (n_end > 0) {
-            if (ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarODone + i), (n_end - 1) & 1))) {
+            if (n >= 1 && __any_sync(0xffffffffu, need)) {
+                // rare: rescale O.  PV(0..n-1) accumulate into O in order; wait for the last.
+                const int pb = (n - 1) % kBufs;
+                if (!__all_sync(0xffffffffu, mbar_wait(BAR(kBarODone + pb), ((n - 1) / kBufs) & 1))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                const float inv = (valid && l_run > 0.f) ? 1.f / l_run : 0.f;
-                uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(cq0 + tok) * p.num_q_heads + head) * kD);
 #pragma unroll
                 for (int c = 0; c < kD / 32; ++c) {
                     uint32_t v[32];
                     tmem_ld32(o_addr + c * 32, v);
                     tmem_wait_ld();
-                    if (valid) {
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv, __uint_as_float(v[8 * k + 1]) * inv);
-                            w.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv);
-                            w.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv);
-                            w.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv);
-                            dst[c * 4 + k] = w;
-                        }
+                    for (int j = 0; j < 32; ++j)
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+                    tmem_st32(o_addr + c * 32, v);
+                }
+            }
+            // P(n) as bf16 pairs over the first 64 columns of buffer bb (A operand of PV(n))
+            tmem_st64(s_addr, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(BAR(kBarPFull + bb));
+        }
+        // ---- epilogue: O / l -> bf16 rows ----
+        const int last = nkv - 1;
+        if (ok && __all_sync(0xffffffffu, mbar_wait(BAR(kBarODone + last % kBufs), (last / kBufs) & 1))) {
+            tc_fence_after();
+            const float inv = (valid && l_run > 0.f) ? 1.f / l_run : 0.f;
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(cq0 + tok) * p.num_q_heads + head) * kD);
+#pragma unroll
+            for (int c = 0; c < kD / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(o_addr + c * 32, v);
+                tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(v[8 * k + 0]) * inv, __uint_as_float(v[8 * k + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(v[8 * k + 2]) * inv, __uint_as_float(v[8 * k + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(v[8 * k + 4]) * inv, __uint_as_float(v[8 * k + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(v[8 * k + 6]) * inv, __uint_as_float(v[8 * k + 7]) * inv);
+                        dst[c * 4 + k] = w;
                     }
                 }
-            } else if (lane == 0) {
-                flag_error(p.d_err, NV_DERR_TIMEOUT);
             }
+        } else if (lane == 0) {
+            flag_error(p.d_err, NV_DERR_TIMEOUT);
         }
     }
 
     // ---------------- teardown: every TMEM access is done before the free ----------------
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -621,9 +594,9 @@ extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const v
     p.block_shift = ilog2(block_size);
     p.box_rows = box_rows;
     p.num_blocks = num_blocks;
-    p.max_pairs = (max_seqlen_q + 2 * tq - 1) / (2 * tq);
+    p.max_tiles = (max_seqlen_q + tq - 1) / tq;
     p.scale_log2 = scale * nvkv::kLog2e;
-    if (p.max_pairs > 65535)
+    if (p.max_tiles > 65535)
         return NV_ERR_UNSUPPORTED;
 
     static std::once_flag attr_once;
@@ -633,7 +606,7 @@ extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const v
     });
     if (attr_err != cudaSuccess)
         return NV_ERR_CUDA;
-    dim3 grid(num_kv_heads, num_seqs, p.max_pairs);
+    dim3 grid(num_kv_heads, num_seqs, p.max_tiles);
     paged_prefill_kernel<<<grid, kThreads, kSmemBytes, (cudaStream_t)stream>>>(tq_map, tk, tv, p);
     return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
