@@ -171,13 +171,20 @@ int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, const void 
  *                 chunk beyond it are not computed and NV_DERR_LENGTH is set.
  *   total_q       cu_seqlens_q[num_seqs] (rows of q and out).
  *   k_cache, v_cache  as above; additionally num_blocks*block_size < 2^31.
+ *   workspace     device scratch of at least NV_PREFILL_WORKSPACE_BYTES bytes, 16-byte aligned,
+ *                 else NV_ERR_WORKSPACE.  It holds the counter from which the persistent CTAs
+ *                 claim query tiles; the call zeroes it on `stream` first, so it needs no
+ *                 initialisation, but calls that share a workspace must not overlap on the device.
  */
+#define NV_PREFILL_WORKSPACE_BYTES 256u
+
 int nv_paged_prefill_attn(const void *q, const void *k_cache, const void *v_cache,
                           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                           const int32_t *block_tables, int32_t bt_stride, int32_t num_seqs,
                           int32_t total_q, int32_t max_seqlen_q, int32_t num_q_heads,
                           int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                          float scale, void *out, int32_t *d_err, nv_stream_t stream);
+                          float scale, void *out, void *workspace, size_t workspace_bytes,
+                          int32_t *d_err, nv_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -88,9 +88,9 @@ def test_decode_validation(lib):
 
 
 def _prefill(lib, q=FAKE, kc=FAKE, vc=FAKE, cq=FAKE, ck=FAKE, bt=FAKE, bts=8, B=2, tq=100, mq=80, hq=16, hkv=8,
-             d=128, bs=256, nb=16, out=FAKE):
-    return lib.nv_paged_prefill_attn(q, kc, vc, cq, ck, bt, bts, B, tq, mq, hq, hkv, d, bs, nb, 0.088, out, None,
-                                     None)
+             d=128, bs=256, nb=16, out=FAKE, ws=FAKE, wsb=256):
+    return lib.nv_paged_prefill_attn(q, kc, vc, cq, ck, bt, bts, B, tq, mq, hq, hkv, d, bs, nb, 0.088, out, ws, wsb,
+                                     None, None)
 
 
 def test_prefill_validation(lib):
@@ -102,6 +102,9 @@ def test_prefill_validation(lib):
     assert _prefill(lib, bs=512) == NV_ERR_UNSUPPORTED
     assert _prefill(lib, kc=MISALIGNED) == NV_ERR_ALIGN
     assert _prefill(lib, nb=0) == NV_ERR_SHAPE
+    assert _prefill(lib, ws=None) == NV_ERR_WORKSPACE
+    assert _prefill(lib, wsb=nv.NV_PREFILL_WORKSPACE_BYTES - 16) == NV_ERR_WORKSPACE
+    assert _prefill(lib, ws=MISALIGNED) == NV_ERR_WORKSPACE
 
 
 @pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="checks the no-GPU path only")
