@@ -299,8 +299,9 @@ def run_ours(args, rank, world, local_rank):
         pslots, pbt = to_dev(pb.slot_mapping), to_dev(pb.block_tables)
         pcu_q, pcu_k = to_dev(pb.cu_seqlens_q), to_dev(pb.cu_seqlens_k)
         pout = torch.empty_like(pq)
-        pws = torch.empty(nv.NV_PREFILL_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
         mq = int(pb.q_lens.max())
+        pws = torch.empty(nv.nv_paged_prefill_workspace_size(pb.num_seqs, int(pb.q_lens.sum()), mq, pb.num_q_heads,
+                                                             pb.num_kv_heads), dtype=torch.uint8, device=dev)
         flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)   # > 129 MB L2
 
         def prefill_step(ev=None):
@@ -390,10 +391,9 @@ def run_ours(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max / args.steps, 4)},
-        "gpu_launches": (launches_per_decode_step * 2 + 2) * args.steps,
+        "gpu_launches": (launches_per_decode_step * 2 + 3) * args.steps,
         "gpu_launches_note": "decode phase: store + split-KV decode + merge per step; "
-                             "e2e phase: same kernels; prefill phase: store + prefill per step (the prefill "
-                             "call also enqueues a 4-byte memset of its tile counter, not counted)",
+                             "e2e phase: same kernels; prefill phase: store + work-list pre-pass + prefill per step",
         "clocks": clocks,
         "prefill": {
             "workload": "chunked prefill with prefix cache (store 16384 new rows + causal varlen prefill): 16 seqs, "

@@ -171,12 +171,23 @@ int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, const void 
  *                 chunk beyond it are not computed and NV_DERR_LENGTH is set.
  *   total_q       cu_seqlens_q[num_seqs] (rows of q and out).
  *   k_cache, v_cache  as above; additionally num_blocks*block_size < 2^31.
- *   workspace     device scratch of at least NV_PREFILL_WORKSPACE_BYTES bytes, 16-byte aligned,
- *                 else NV_ERR_WORKSPACE.  It holds the counter from which the persistent CTAs
- *                 claim query tiles; the call zeroes it on `stream` first, so it needs no
- *                 initialisation, but calls that share a workspace must not overlap on the device.
+ *   workspace     device scratch of at least nv_paged_prefill_workspace_size(...) bytes,
+ *                 16-byte aligned, else NV_ERR_WORKSPACE.  The call first writes into it (on
+ *                 `stream`, a one-CTA pre-pass) the list of query tiles, heaviest first, and the
+ *                 counter from which the persistent CTAs claim them, so it needs no
+ *                 initialisation; calls that share a workspace must not overlap on the device.
+ *                 A batch whose tiles would not fit (cu_seqlens_q inconsistent with total_q) sets
+ *                 NV_DERR_LENGTH and leaves the lightest tiles uncomputed.
+ * Enqueues two kernels: the pre-pass and the attention kernel.
  */
-#define NV_PREFILL_WORKSPACE_BYTES 256u
+
+/*
+ * Bytes of workspace nv_paged_prefill_attn needs: 64 + 32 bytes per query tile of 128/G rows
+ * (G = num_q_heads / num_kv_heads), for at most min(ceil(total_q*G/128) + num_seqs,
+ * num_seqs * ceil(max_seqlen_q*G/128)) tiles.  Depends only on its arguments.
+ */
+size_t nv_paged_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
+                                       int32_t num_q_heads, int32_t num_kv_heads);
 
 int nv_paged_prefill_attn(const void *q, const void *k_cache, const void *v_cache,
                           const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,

@@ -28,10 +28,8 @@ NV_DERR_BLOCK_RANGE = 0x2
 NV_DERR_LENGTH = 0x4
 NV_DERR_TIMEOUT = 0x8
 
-NV_PREFILL_WORKSPACE_BYTES = 256
-
 EXPORTED = ("nv_status_string", "nv_store_kvcache", "nv_paged_decode_workspace_size", "nv_paged_decode_attn",
-            "nv_paged_decode_attn_noalloc", "nv_paged_prefill_attn")
+            "nv_paged_decode_attn_noalloc", "nv_paged_prefill_workspace_size", "nv_paged_prefill_attn")
 
 
 class NvError(RuntimeError):
@@ -67,6 +65,8 @@ def load_library(path: str | None = None):
     L.nv_paged_decode_attn.restype = ctypes.c_int
     L.nv_paged_decode_attn_noalloc.argtypes = [V, V, V, V, i32, V, i32, i32, i32, i32, i32, i32, i32, f32, V, V, V]
     L.nv_paged_decode_attn_noalloc.restype = ctypes.c_int
+    L.nv_paged_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    L.nv_paged_prefill_workspace_size.restype = sz
     L.nv_paged_prefill_attn.argtypes = [V, V, V, V, V, V, i32, i32, i32, i32, i32, i32, i32, i32, i32, f32, V, V, sz,
                                         V, V]
     L.nv_paged_prefill_attn.restype = ctypes.c_int
@@ -172,13 +172,18 @@ def nv_paged_decode_attn_noalloc(q, k_cache, v_cache, block_tables, context_lens
     return out
 
 
+def nv_paged_prefill_workspace_size(num_seqs, total_q, max_seqlen_q, num_q_heads, num_kv_heads) -> int:
+    return int(load_library().nv_paged_prefill_workspace_size(num_seqs, total_q, max_seqlen_q, num_q_heads,
+                                                              num_kv_heads))
+
+
 def nv_paged_prefill_attn(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block_tables, scale, max_seqlen_q=None,
                           out=None, workspace=None, d_err=None, stream=None):
     """Causal varlen prefill: packed ``q`` ``[total_q, Hq, D]`` over cached prefix + chunk.
 
-    ``max_seqlen_q`` (host int) sizes the work list; by default ``total_q``, an upper bound that
-    needs no device read (tiles past a chunk's end are skipped).  ``workspace`` (at least
-    ``NV_PREFILL_WORKSPACE_BYTES`` bytes) is allocated with torch when not given."""
+    ``max_seqlen_q`` (host int) bounds every chunk's length; by default ``total_q``, an upper
+    bound that needs no device read.  ``workspace`` (``nv_paged_prefill_workspace_size`` bytes)
+    is allocated with torch when not given."""
     import torch
     nb, bs, hkv, d = _pool_shape(k_cache, v_cache)
     total_q, hq, dq = (int(x) for x in q.shape)
@@ -189,12 +194,14 @@ def nv_paged_prefill_attn(q, k_cache, v_cache, cu_seqlens_q, cu_seqlens_k, block
           "block_tables must be [B, W] with unit column stride")
     if out is None:
         out = torch.empty_like(q)
-    if workspace is None:
-        workspace = torch.empty(NV_PREFILL_WORKSPACE_BYTES, dtype=torch.uint8, device=q.device)
-    ws_bytes = workspace.numel() * workspace.element_size()
+    mq = int(total_q if max_seqlen_q is None else max_seqlen_q)
+    if workspace is None and B > 0 and total_q > 0 and mq > 0:
+        workspace = torch.empty(nv_paged_prefill_workspace_size(B, total_q, mq, hq, hkv), dtype=torch.uint8,
+                                device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load_library().nv_paged_prefill_attn(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(block_tables),
-        block_tables.stride(0), B, total_q, int(total_q if max_seqlen_q is None else max_seqlen_q), hq, hkv, d, bs,
-        nb, float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_err), _stream(stream))
+        block_tables.stride(0), B, total_q, mq, hq, hkv, d, bs, nb, float(scale), _ptr(out), _ptr(workspace),
+        ws_bytes, _ptr(d_err), _stream(stream))
     _check("nv_paged_prefill_attn", rc)
     return out

@@ -11,6 +11,8 @@
 // is persistent (one CTA per SM): CTAs claim tiles, heaviest first, from a counter in the
 // caller's workspace, and each CTA runs its tiles as one continuous stream of 128-key steps, so
 // the next tile's first scores are computed while the current tile finishes.
+//   * a one-CTA pre-pass lists the non-empty query tiles, heaviest first (counting sort by
+//     128-key steps), in the caller's workspace; a claim is one atomic add on a counter there.
 //   * warp 4 (TMA producer): claims tiles and passes them to the other warps through a small
 //     queue in shared memory.  Copies go out in the order they are needed: a tile's Q (one 3-D
 //     tensor-map copy per 64-dim half; dims head_dim, q head, token) into one of two Q buffers,
@@ -18,13 +20,15 @@
 //     head, slot), 128-byte swizzled, into a 3-slot K ring and a 2-slot V ring, K running two
 //     steps ahead of V as the MMAs consume them.  Lane i copies box i of a step; the block-table
 //     row is held 32 entries at a time in the warp's registers.
-//   * warp 5 (MMA issuer; owns the TMEM allocation): one lane issues tcgen05.mma kind::f16
-//     with fp32 accumulators in tensor memory.  TMEM holds THREE score buffers of 128 columns
-//     and the 128-column O accumulator.  S(n) = Q K(n)^T (operands in shared memory) goes to
-//     buffer n % 3; the softmax writes P(n) as bf16 pairs over the first half of that buffer;
-//     O += P(n) V(n) reads P from tensor memory.  S(n+2) is issued right after PV(n): its
-//     buffer last held P(n-1), whose PV finished an iteration earlier, so the issuer never
-//     waits on a group it has just queued.  Operand descriptors are precomputed per buffer.
+//   * warps 5 and 6 (MMA issuers; warp 5 owns the TMEM allocation): one lane of warp 5 issues
+//     S(n) = Q K(n)^T (operands in shared memory), one lane of warp 6 issues O += P(n) V(n)
+//     (P read from tensor memory), tcgen05.mma kind::f16 with fp32 accumulators.  TMEM holds
+//     THREE score buffers of 128 columns and the 128-column O accumulator; S(n) goes to buffer
+//     n % 3, where the softmax then writes P(n) as bf16 pairs over the first half.  S(n) may be
+//     issued as soon as PV(n-3) has freed its buffer.  The MMA issue queue is shallow, so any
+//     latency in the issuing thread (barrier waits, commits, bookkeeping) idles the tensor pipe;
+//     with two issuers one warp's waits overlap the other's MMAs (a single alternating issuer
+//     measured 25% slower).  Operand descriptors are precomputed per buffer.
 //   * warps 0-3 (softmax / correction / epilogue): thread r owns row r = TMEM lane r.  It loads
 //     its 128 scores at once, masks only on steps that cross the diagonal (a separate code
 //     path), keeps a base-2 online softmax with a lazy rescale (the running max moves only when
@@ -32,8 +36,7 @@
 //     tcgen05.st.  At a tile's end it normalises O, stages the bf16 rows in the tile's Q buffer
 //     (free once the last PV is done) and writes them with tensor-map stores.
 // Measured on GB300: an M=128 tcgen05.mma costs about the same for N=64 as for N=128 (so key
-// steps are 128 wide), the MMA issue queue is shallow (any idle time in the issuing warp idles
-// the tensor pipe), and loading 128 fp32 scores from TMEM takes ~100 cycles.
+// steps are 128 wide), and loading 128 fp32 scores from TMEM takes ~100 cycles.
 // Every mbarrier wait is bounded; on timeout the kernel records NV_DERR_TIMEOUT and stops.
 #include <cuda.h>
 
@@ -56,7 +59,12 @@ constexpr int kQBufs = 2;            // Q buffers: the next item's Q loads while
 constexpr int kKSlots = NVKV_PREFILL_KSLOTS;   // K ring slots
 constexpr int kVSlots = 5 - kKSlots;           // V ring slots
 constexpr int kBufs = 3;             // score / P buffers in TMEM
-constexpr int kThreads = 192;        // warps 0-3 softmax; 4 producer; 5 MMA
+#ifndef NVKV_PREFILL_DUAL
+#define NVKV_PREFILL_DUAL 1
+#endif
+// Two MMA-issuing warps (5: S = Q K^T, 6: O += P V) or one (5) that alternates them.
+constexpr bool kDualIssuer = NVKV_PREFILL_DUAL != 0;
+constexpr int kThreads = kDualIssuer ? 224 : 192;    // warps 0-3 softmax; 4 producer; 5 (and 6) MMA
 constexpr uint32_t kTmemCols = 512;  // buffer b at b*128, O at 384
 constexpr uint32_t kTmemO = 384;
 constexpr float kRescaleLog2 = 8.0f;
@@ -76,26 +84,23 @@ constexpr uint32_t kOffBar = kOffV + kVSlots * kTile;
 constexpr int kBarQFull = 0;                       // + q buffer
 constexpr int kBarQEmpty = 2;                      // + q buffer
 constexpr int kBarKFull = 4;                       // + K slot
-constexpr int kBarKEmpty = kBarKFull + kKSlots;    // + K slot
-constexpr int kBarVFull = kBarKEmpty + kKSlots;    // + V slot
-constexpr int kBarVEmpty = kBarVFull + kVSlots;    // + V slot
-constexpr int kBarSFull = kBarVEmpty + kVSlots;    // + buffer
+constexpr int kBarVFull = kBarKFull + kKSlots;     // + V slot
+constexpr int kBarSFull = kBarVFull + kVSlots;     // + buffer (also: K slot of that S is free)
 constexpr int kBarPFull = kBarSFull + kBufs;       // + buffer
-constexpr int kBarODone = kBarPFull + kBufs;       // + buffer (PV(n) commits to n % 3)
+constexpr int kBarODone = kBarPFull + kBufs;       // + buffer (PV(n) commits to n % 3; its V slot is free)
 constexpr int kQueue = 8;                          // claimed work items in flight
+constexpr int kItemInts = 12;                      // one work item in the shared-memory queue
 constexpr int kBarItemFull = kBarODone + kBufs;    // + queue slot
 constexpr int kBarItemEmpty = kBarItemFull + kQueue;
-constexpr int kItemReaders = 6;                    // MMA S cursor, MMA PV cursor, 4 softmax warps
+constexpr int kItemReaders = 6;                    // S cursor, PV cursor, 4 softmax warps
 constexpr int kNumBars = kBarItemEmpty + kQueue;
 constexpr uint32_t kOffItems = kOffBar + kNumBars * 8;
-constexpr uint32_t kOffTmemSlot = kOffItems + kQueue * 4;
+constexpr uint32_t kOffTmemSlot = kOffItems + kQueue * kItemInts * 4;
 constexpr uint32_t kSmemBytes = kOffTmemSlot + 16 + 1024;      // + slack for 1024-byte alignment
 static_assert(kSmemBytes <= 227u * 1024u, "shared memory per CTA");
 
 struct PrefillParams {
     __nv_bfloat16 *out;
-    const int32_t *cu_q;
-    const int32_t *cu_k;
     const int32_t *block_tables;
     int32_t *d_err;
     int32_t bt_stride;
@@ -105,10 +110,8 @@ struct PrefillParams {
     int32_t block_shift;    // log2 block_size
     int32_t box_rows;       // min(block_size, kBN)
     int32_t num_blocks;
-    int32_t max_tiles;      // query tiles of the longest chunk
     int32_t num_kv_heads;
-    int32_t num_seqs;
-    int32_t *tile_counter;  // zeroed before the launch; CTAs claim work items from it
+    int32_t *ws;            // work list written by the pre-pass: [0] claim counter, [1] entries
     float scale_log2;
 };
 
@@ -208,56 +211,134 @@ __device__ __forceinline__ float exp_pack64(const float (&s)[64], float scale_lo
     return (ra + rb) + (rc + rd);
 }
 
-// One unit of work: a 128-row query tile of one (sequence, kv head).  Virtual tile v runs over
-// (tile level, sequence, kv head) with the tile level slowest and counted from the LAST tile of
-// the longest chunk, so the heaviest tiles (most keys) come first.  Persistent CTAs claim them
-// in that order from a global counter and skip those past the end of their sequence's chunk.
+// One unit of work: a 128-row query tile of one (sequence, kv head).
 struct Item {
-    int v;
+    int v;                  // claim number; >= total marks the end of the work
     int b, kvh, cq0, Lq, P, i0, nq, kv_len, nkv, first_masked;
 };
 
-__device__ __forceinline__ bool load_item(const PrefillParams &p, int v, Item &it)
+// ---------------------------------------------------------------------------------------
+// Work list.  A one-CTA pre-pass lists every non-empty query tile of every sequence (all kv
+// heads share an entry) in the workspace, ordered by its number of 128-key steps, heaviest
+// first (a counting sort), validates the lengths, and zeroes the claim counter.  The main
+// kernel's claim number v then names entry v / Hkv and kv head v % Hkv: a claim is one atomic
+// add and one 32-byte record load, with no empty tiles to skip.
+//   workspace ints: [0] claim counter, [1] entries, [16 + 8e ...] entry e:
+//   {b, cq0, Lq, P, i0, nq, kv_len, nkv}
+// ---------------------------------------------------------------------------------------
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanBuckets = 8192;  // by 128-key steps; heavier tiles share the last bucket
+constexpr int kPlanHeaderInts = 16;
+
+struct PlanParams {
+    const int32_t *cu_q;
+    const int32_t *cu_k;
+    int32_t *ws;
+    int32_t *d_err;
+    int32_t num_seqs, total_q, bt_stride, block_shift, tq, max_tiles, cap;
+};
+
+__device__ __forceinline__ bool plan_seq(const PlanParams &pp, int b, int &cq0, int &Lq, int &P, int &T)
 {
-    const int per_level = p.num_seqs * p.num_kv_heads;
-    const int level = v / per_level;
-    const int rem = v - level * per_level;
-    it.v = v;
-    it.b = rem / p.num_kv_heads;
-    it.kvh = rem - it.b * p.num_kv_heads;
-    it.cq0 = __ldg(p.cu_q + it.b);
-    const int cq1 = __ldg(p.cu_q + it.b + 1);
-    const int Lk = __ldg(p.cu_k + it.b + 1) - __ldg(p.cu_k + it.b);
-    it.Lq = cq1 - it.cq0;
-    it.P = Lk - it.Lq;
-    if (it.Lq < 0 || it.P < 0 || ((Lk + (1 << p.block_shift) - 1) >> p.block_shift) > p.bt_stride) {
-        flag_error(p.d_err, NV_DERR_LENGTH);
+    cq0 = pp.cu_q[b];
+    const int cq1 = pp.cu_q[b + 1];
+    const int Lk = pp.cu_k[b + 1] - pp.cu_k[b];
+    Lq = cq1 - cq0;
+    P = Lk - Lq;
+    if (Lq < 0 || P < 0 || cq0 < 0 || cq1 > pp.total_q ||
+        ((Lk + (1 << pp.block_shift) - 1) >> pp.block_shift) > pp.bt_stride) {
+        flag_error(pp.d_err, NV_DERR_LENGTH);
         return false;
     }
-    const int tq = kBM >> p.group_shift;
-    const int ntiles = (it.Lq + tq - 1) / tq;
-    if (level == 0 && ntiles > p.max_tiles)
-        flag_error(p.d_err, NV_DERR_LENGTH);
-    const int tile = p.max_tiles - 1 - level;
-    if (tile >= ntiles)
-        return false;
-    it.i0 = tile * tq;
-    it.nq = min(tq, it.Lq - it.i0);
-    it.kv_len = it.P + it.i0 + it.nq;
-    it.nkv = (it.kv_len + kBN - 1) / kBN;
-    it.first_masked = (it.P + it.i0 + 1) / kBN;
+    const int nt = (Lq + pp.tq - 1) / pp.tq;
+    if (nt > pp.max_tiles)
+        flag_error(pp.d_err, NV_DERR_LENGTH);
+    T = min(nt, pp.max_tiles);
     return true;
 }
 
-// Resolve a claimed virtual tile: while it is empty (past its chunk's end), claim the next one
-// from the global counter.  Returns total when none is left.  Tiles are claimed in the
-// heaviest-first order as CTAs free up, which balances the load.
-__device__ __forceinline__ int resolve_claim(const PrefillParams &p, int v, int total)
+__device__ __forceinline__ int tile_steps(int P, int Lq, int i0, int tq)
 {
-    Item it;
-    while (v < total && !load_item(p, v, it))
-        v = atomicAdd(p.tile_counter, 1);
-    return v < total ? v : total;
+    return (P + i0 + min(tq, Lq - i0) + kBN - 1) / kBN;
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const PlanParams pp)
+{
+    __shared__ int hist[kPlanBuckets];
+    __shared__ int warp_tot[kPlanThreads / 32];
+    __shared__ int count;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < kPlanBuckets; i += kPlanThreads)
+        hist[i] = 0;
+    __syncthreads();
+    for (int b = tid; b < pp.num_seqs; b += kPlanThreads) {
+        int cq0, Lq, P, T;
+        if (plan_seq(pp, b, cq0, Lq, P, T))
+            for (int t = 0; t < T; ++t)
+                atomicAdd(&hist[min(tile_steps(P, Lq, t * pp.tq, pp.tq), kPlanBuckets - 1)], 1);
+    }
+    __syncthreads();
+    // exclusive prefix sum with the buckets in DESCENDING order: thread tid owns 8 of them
+    constexpr int kPer = kPlanBuckets / kPlanThreads;
+    int loc[kPer];
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        loc[j] = hist[kPlanBuckets - 1 - (tid * kPer + j)];
+        sum += loc[j];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    if (lane == 31)
+        warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o)
+                w += y;
+        }
+        warp_tot[lane] = w;             // inclusive over warps
+        if (lane == 31)
+            count = w;
+    }
+    __syncthreads();
+    int run = incl - sum + (warp > 0 ? warp_tot[warp - 1] : 0);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        hist[kPlanBuckets - 1 - (tid * kPer + j)] = run;
+        run += loc[j];
+    }
+    __syncthreads();
+    int4 *rec = reinterpret_cast<int4 *>(pp.ws + kPlanHeaderInts);
+    for (int b = tid; b < pp.num_seqs; b += kPlanThreads) {
+        int cq0, Lq, P, T;
+        if (!plan_seq(pp, b, cq0, Lq, P, T))
+            continue;
+        for (int t = 0; t < T; ++t) {
+            const int i0 = t * pp.tq;
+            const int nkv = tile_steps(P, Lq, i0, pp.tq);
+            const int e = atomicAdd(&hist[min(nkv, kPlanBuckets - 1)], 1);
+            if (e < pp.cap) {
+                const int nq = min(pp.tq, Lq - i0);
+                rec[2 * e] = make_int4(b, cq0, Lq, P);
+                rec[2 * e + 1] = make_int4(i0, nq, P + i0 + nq, nkv);
+            }
+        }
+    }
+    if (tid == 0) {
+        if (count > pp.cap)
+            flag_error(pp.d_err, NV_DERR_LENGTH);
+        pp.ws[0] = 0;
+        pp.ws[1] = min(count, pp.cap);
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -272,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int total = p.max_tiles * p.num_seqs * p.num_kv_heads;
+    const int total = p.ws[1] * p.num_kv_heads;      // claims: work-list entries x kv heads
 
     const uint32_t bar = base + kOffBar;
     auto BAR = [&](int i) { return bar + 8u * (uint32_t)i; };
@@ -285,11 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < kKSlots; ++s) {
             mbar_init(BAR(kBarKFull + s), 1);
-            mbar_init(BAR(kBarKEmpty + s), 1);
         }
         for (int s = 0; s < kVSlots; ++s) {
             mbar_init(BAR(kBarVFull + s), 1);
-            mbar_init(BAR(kBarVEmpty + s), 1);
         }
         for (int s = 0; s < kBufs; ++s) {
             mbar_init(BAR(kBarSFull + s), 1);
@@ -305,10 +384,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Work items pass from the producer (which claims them) to the MMA issuer's two cursors and
     // the four softmax warps through a small queue in shared memory.
     volatile int *items = reinterpret_cast<volatile int *>(smem + kOffItems);
-    auto read_item = [&](int k, int &v) {            // whole warp calls; lane 0 releases the slot
+    auto read_item = [&](int k, Item &it) {          // whole warp calls; lane 0 releases the slot
         if (!__all_sync(0xffffffffu, mbar_wait(BAR(kBarItemFull + k % kQueue), (k / kQueue) & 1)))
             return false;
-        v = items[k % kQueue];
+        volatile int *q = items + (k % kQueue) * kItemInts;
+        it.v = q[0];
+        it.b = q[1];
+        it.kvh = q[2];
+        it.cq0 = q[3];
+        it.Lq = q[4];
+        it.P = q[5];
+        it.i0 = q[6];
+        it.nq = q[7];
+        it.kv_len = q[8];
+        it.nkv = q[9];
+        it.first_masked = q[10];
         __syncwarp();
         if (lane == 0)
             mbar_arrive(BAR(kBarItemEmpty + k % kQueue));
@@ -343,14 +433,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             int kvh;
             uint32_t bytes;     // whole tile
         };
-        // copy one K or V tile into its ring (idx = its global key tile)
+        // copy one K or V tile into its ring (idx = its global key tile).  The slot's previous
+        // tile (idx - slots) is free once its MMA group has completed: S for K, PV for V, whose
+        // commits to the score-buffer barriers already signal that.
         auto copy_tile = [&](bool is_v, int idx, const TileCopy &c) {
             const int n_slots = is_v ? kVSlots : kKSlots;
             const int s_ = idx % n_slots;
             const uint32_t full = BAR((is_v ? kBarVFull : kBarKFull) + s_);
-            if (idx >= n_slots &&
+            const int prev = idx - n_slots;
+            if (prev >= 0 &&
                 !__all_sync(0xffffffffu,
-                            mbar_wait(BAR((is_v ? kBarVEmpty : kBarKEmpty) + s_), ((idx / n_slots) - 1) & 1)))
+                            mbar_wait(BAR((is_v ? kBarODone : kBarSFull) + prev % kBufs), (prev / kBufs) & 1)))
                 return false;
             const uint32_t dst = base + (is_v ? kOffV : kOffK) + s_ * kTile + (uint32_t)lane * p.box_rows * 128u;
             if (lane == 0)
@@ -367,30 +460,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         int j = 0;                                  // global key tile of the next K copy
         TileCopy v1{-1, 0, 0}, v2{-1, 0, 0};        // tiles j-1 and j-2, whose V is still to copy
         // lane 0 claims one item ahead: the counter's answer for item k+1 travels while item k's
-        // copies are issued, and is resolved (empty tiles skipped) only when it is needed
+        // copies are issued
+        const int4 *plan = reinterpret_cast<const int4 *>(p.ws + kPlanHeaderInts);
         int pending = 0;
         if (lane == 0)
-            pending = atomicAdd(p.tile_counter, 1);
+            pending = atomicAdd(p.ws, 1);
         for (int k = 0; ok; ++k) {
-            // publish item k to the other warps
+            // item k: its claim number, then its work-list entry (lanes 0-1 load the two halves)
             if (k >= kQueue &&
                 !__all_sync(0xffffffffu, mbar_wait(BAR(kBarItemEmpty + k % kQueue), ((k / kQueue) - 1) & 1))) {
                 ok = false;
                 break;
             }
-            int v = 0;
-            if (lane == 0) {
-                v = resolve_claim(p, pending, total);
-                items[k % kQueue] = v;
-                mbar_arrive(BAR(kBarItemFull + k % kQueue));
-                if (v < total)
-                    pending = atomicAdd(p.tile_counter, 1);
+            const int v = __shfl_sync(0xffffffffu, pending, 0);
+            if (lane == 0 && v < total)
+                pending = atomicAdd(p.ws, 1);
+            Item it{};
+            it.v = v < total ? v : total;
+            if (v < total) {
+                const int e = v / p.num_kv_heads;
+                int4 r = make_int4(0, 0, 0, 0);
+                if (lane < 2)
+                    r = plan[2 * e + lane];
+                it.b = __shfl_sync(0xffffffffu, r.x, 0);
+                it.cq0 = __shfl_sync(0xffffffffu, r.y, 0);
+                it.Lq = __shfl_sync(0xffffffffu, r.z, 0);
+                it.P = __shfl_sync(0xffffffffu, r.w, 0);
+                it.i0 = __shfl_sync(0xffffffffu, r.x, 1);
+                it.nq = __shfl_sync(0xffffffffu, r.y, 1);
+                it.kv_len = __shfl_sync(0xffffffffu, r.z, 1);
+                it.nkv = __shfl_sync(0xffffffffu, r.w, 1);
+                it.kvh = v - e * p.num_kv_heads;
+                it.first_masked = (it.P + it.i0 + 1) / kBN;
             }
-            v = __shfl_sync(0xffffffffu, v, 0);
+            if (lane == 0) {
+                volatile int *q = items + (k % kQueue) * kItemInts;
+                q[0] = it.v;
+                q[1] = it.b;
+                q[2] = it.kvh;
+                q[3] = it.cq0;
+                q[4] = it.Lq;
+                q[5] = it.P;
+                q[6] = it.i0;
+                q[7] = it.nq;
+                q[8] = it.kv_len;
+                q[9] = it.nkv;
+                q[10] = it.first_masked;
+                mbar_arrive(BAR(kBarItemFull + k % kQueue));
+            }
             if (v >= total)
                 break;
-            Item it;
-            load_item(p, v, it);
             const int32_t *bt = p.block_tables + (size_t)it.b * p.bt_stride;
             const int nblk = (it.kv_len + (1 << p.block_shift) - 1) >> p.block_shift;
             int win_base = 0;                       // the block-table row, 32 entries at a time
@@ -454,11 +573,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = copy_tile(true, j - 1, v1);
         if (!ok && lane == 0)
             flag_error(p.d_err, NV_DERR_TIMEOUT);
-    } else if (warp == 5) {
-        // ============================ MMA issuer ============================
-        // Key tiles of all this CTA's work items form one global sequence g.  S(g) goes to TMEM
-        // buffer g % 3; the issue order S(0) S(1) | PV(g) S(g+2) | ... runs across tile boundaries,
-        // so the next tile's first scores are computed during the current tile's last softmax.
+    } else if (warp == 5 || warp == 6) {
+        // ============================ MMA issuer(s) ============================
+        // Key steps of all this CTA's work items form one global sequence g.  S(g) goes to TMEM
+        // buffer g % 3 once PV(g-3) has finished with it; both streams run across tile
+        // boundaries, so the next tile's first scores are computed during the current tile's last
+        // softmax.  (Single-issuer build: the order S(0) S(1) | PV(g) S(g+2) | ...)
         constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);   // Q, K both K-major
         constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kD, false, true);     // P (TMEM), V MN-major
         // Operand descriptors of Q buffer 0 and K / V slot 0; the others differ only in the start
@@ -483,14 +603,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the cursor reaches it, so the issuer never waits for a claim it does not yet need
         auto ready = [&](Cursor &c) {
             if (!c.have) {
-                int v = total;
-                if (!read_item(c.k, v)) {
+                if (!read_item(c.k, c.it)) {
                     ok = false;
-                    v = total;
+                    c.it.v = total;
                 }
-                c.it.v = v;
-                if (v < total)
-                    load_item(p, v, c.it);
                 c.have = true;
             }
             return ok && c.it.v < total;
@@ -527,7 +643,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16_ss(tmem + bb * 128, dq + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(BAR(kBarSFull + bb));
-                mma_commit(BAR(kBarKEmpty + slot));
                 if (c.n == c.it.nkv - 1)
                     mma_commit(BAR(kBarQEmpty + qb));   // the item's last use of its Q buffer
             }
@@ -542,17 +657,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_all(BAR(kBarVFull + slot), (g / kVSlots) & 1))
                 return;
             const uint32_t vtile = base + kOffV + slot * kTile;
-            const int vrows = c.it.kv_len - n * kBN;
+            // Keys past the sequence carry P = 0, but their V rows may hold anything (NaN patterns
+            // included) and 0 * NaN would poison O: zero them.  (Skipping their k-steps instead
+            // measured slower.)
+            const int vrows = min(c.it.kv_len - n * kBN, kBN);
             if (vrows < kBN) {
-                // Keys past the sequence carry P = 0, but their V rows may hold anything (NaN
-                // patterns included) and 0 * NaN would poison O: zero them.
-                const int per_half = (kBN - vrows) * 8;        // 16-byte chunks
-                for (int c2 = lane; c2 < 2 * per_half; c2 += 32) {
-                    const int half = c2 / per_half;
-                    const int rem = c2 % per_half;
-                    sts_u4(vtile + half * kHalf + (uint32_t)(vrows + rem / 8) * 128u + (uint32_t)(rem % 8) * 16u,
+                for (int c2 = lane; c2 < (kBN - vrows) * 16; c2 += 32)     // 16-byte chunk: row, half, column
+                    sts_u4(vtile + ((c2 >> 3) & 1) * kHalf + (uint32_t)(vrows + (c2 >> 4)) * 128u +
+                               (uint32_t)(c2 & 7) * 16u,
                            make_uint4(0, 0, 0, 0));
-                }
                 fence_proxy_async_smem();
                 __syncwarp();
             }
@@ -566,20 +679,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16_ts(tmem + kTmemO, tmem + bb * 128 + kk * 8, dv + (uint64_t)(kk * 16 * 128 >> 4),
                                 idesc_o, (n > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(BAR(kBarODone + bb));
-                mma_commit(BAR(kBarVEmpty + slot));
             }
             __syncwarp();
             advance(c);
         };
-        // S runs two key tiles ahead of PV
-        if (ready(cs))
-            issue_s(cs);
-        if (ready(cs))
-            issue_s(cs);
-        while (ready(cp)) {
-            issue_pv(cp);
+        if (kDualIssuer) {
+            // each warp streams its own groups; S(g) goes as soon as PV(g-3) has freed its buffer
+            if (warp == 5) {
+                while (ready(cs))
+                    issue_s(cs);
+            } else {
+                while (ready(cp))
+                    issue_pv(cp);
+            }
+        } else {
+            // S runs two key tiles ahead of PV
             if (ready(cs))
                 issue_s(cs);
+            if (ready(cs))
+                issue_s(cs);
+            while (ready(cp)) {
+                issue_pv(cp);
+                if (ready(cs))
+                    issue_s(cs);
+            }
         }
         if (!ok && lane == 0)
             flag_error(p.d_err, NV_DERR_TIMEOUT);
@@ -592,14 +715,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int g = 0;                                      // global key tile
         for (int k = 0; ok; ++k) {
-            int v = total;
-            if (!read_item(k, v)) {
+            if (!read_item(k, it)) {
                 ok = false;
                 break;
             }
-            if (v >= total)
+            if (it.v >= total)
                 break;
-            load_item(p, v, it);
             const int tok = it.i0 + (r >> p.group_shift);   // token index inside the chunk
             const int head = it.kvh * p.group + (r & (p.group - 1));
             const bool valid = tok < it.Lq;
@@ -776,6 +897,34 @@ bool make_map(CUtensorMap *map, const void *base, int64_t rows, int heads, int b
 
 }  // namespace
 
+namespace {
+// Upper bound on the work list's entries: sum_b ceil(Lq_b / tq) <= ceil(total_q / tq) + num_seqs,
+// and no sequence lists more than ceil(max_seqlen_q / tq) tiles.
+int64_t prefill_entries_cap(int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q, int group)
+{
+    const int64_t tq = kBM / group;
+    const int64_t a = (total_q + tq - 1) / tq + num_seqs;
+    const int64_t b = (int64_t)num_seqs * ((max_seqlen_q + tq - 1) / tq);
+    return a < b ? a : b;
+}
+size_t prefill_workspace_bytes(int64_t cap)
+{
+    return (size_t)kPlanHeaderInts * 4u + (size_t)cap * 32u;
+}
+}  // namespace
+
+extern "C" size_t nv_paged_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
+                                                  int32_t num_q_heads, int32_t num_kv_heads)
+{
+    if (num_seqs <= 0 || total_q <= 0 || max_seqlen_q <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0)
+        return (size_t)kPlanHeaderInts * 4u;
+    const int group = num_q_heads / num_kv_heads;
+    if (group > kBM)
+        return (size_t)kPlanHeaderInts * 4u;
+    return prefill_workspace_bytes(prefill_entries_cap(num_seqs, total_q, max_seqlen_q, group));
+}
+
 extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const void *v_cache,
                                      const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                                      const int32_t *block_tables, int32_t bt_stride, int32_t num_seqs,
@@ -807,7 +956,10 @@ extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const v
         return NV_ERR_ALIGN;
     if (num_blocks == 0)
         return NV_ERR_SHAPE;
-    if (!workspace || workspace_bytes < NV_PREFILL_WORKSPACE_BYTES || !aligned16(workspace))
+    const int64_t cap = prefill_entries_cap(num_seqs, total_q, max_seqlen_q, group);
+    if (cap * num_kv_heads >= (1ll << 31))
+        return NV_ERR_UNSUPPORTED;
+    if (!workspace || workspace_bytes < prefill_workspace_bytes(cap) || !aligned16(workspace))
         return NV_ERR_WORKSPACE;
 
     const int box_rows = block_size < kBN ? block_size : kBN;
@@ -822,8 +974,6 @@ extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const v
 
     PrefillParams p{};
     p.out = static_cast<__nv_bfloat16 *>(out);
-    p.cu_q = cu_seqlens_q;
-    p.cu_k = cu_seqlens_k;
     p.block_tables = block_tables;
     p.d_err = d_err;
     p.bt_stride = bt_stride;
@@ -833,18 +983,26 @@ extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const v
     p.block_shift = ilog2(block_size);
     p.box_rows = box_rows;
     p.num_blocks = num_blocks;
-    p.max_tiles = (max_seqlen_q + tq - 1) / tq;
     p.num_kv_heads = num_kv_heads;
-    p.num_seqs = num_seqs;
     p.scale_log2 = scale * nvkv::kLog2e;
-    const int64_t total = (int64_t)p.max_tiles * num_seqs * num_kv_heads;
-    if (total >= (1ll << 31))
-        return NV_ERR_UNSUPPORTED;
+    p.ws = static_cast<int32_t *>(workspace);
+
+    PlanParams pp{};
+    pp.cu_q = cu_seqlens_q;
+    pp.cu_k = cu_seqlens_k;
+    pp.ws = p.ws;
+    pp.d_err = d_err;
+    pp.num_seqs = num_seqs;
+    pp.total_q = total_q;
+    pp.bt_stride = bt_stride;
+    pp.block_shift = p.block_shift;
+    pp.tq = tq;
+    pp.max_tiles = (max_seqlen_q + tq - 1) / tq;
+    pp.cap = (int32_t)cap;
+
     const int sms = sm_count();
     if (sms <= 0)
         return NV_ERR_CUDA;
-    p.tile_counter = static_cast<int32_t *>(workspace);
-
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -852,11 +1010,11 @@ extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const v
     });
     if (attr_err != cudaSuccess)
         return NV_ERR_CUDA;
-    // persistent: one CTA per SM (shared memory and TMEM admit one); CTAs claim tiles of the
-    // heaviest-first order from the counter in the workspace
-    const int grid = (int)(total < sms ? total : sms);
-    if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), (cudaStream_t)stream) != cudaSuccess)
-        return NV_ERR_CUDA;
+    prefill_plan_kernel<<<1, kPlanThreads, 0, (cudaStream_t)stream>>>(pp);
+    // persistent: one CTA per SM (shared memory and TMEM admit one); CTAs claim the work list's
+    // entries heaviest first
+    const int64_t claims = cap * num_kv_heads;
+    const int grid = (int)(claims < sms ? claims : sms);
     paged_prefill_kernel<<<grid, kThreads, kSmemBytes, (cudaStream_t)stream>>>(tq_map, tk, tv, to, p);
     return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }

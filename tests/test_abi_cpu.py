@@ -103,7 +103,9 @@ def test_prefill_validation(lib):
     assert _prefill(lib, kc=MISALIGNED) == NV_ERR_ALIGN
     assert _prefill(lib, nb=0) == NV_ERR_SHAPE
     assert _prefill(lib, ws=None) == NV_ERR_WORKSPACE
-    assert _prefill(lib, wsb=nv.NV_PREFILL_WORKSPACE_BYTES - 16) == NV_ERR_WORKSPACE
+    need = lib.nv_paged_prefill_workspace_size(2, 100, 80, 16, 8)
+    assert need == 64 + 32 * 4                               # min(ceil(100/64) + 2, 2 * ceil(80/64)) tiles
+    assert _prefill(lib, wsb=need - 16) == NV_ERR_WORKSPACE
     assert _prefill(lib, ws=MISALIGNED) == NV_ERR_WORKSPACE
 
 
