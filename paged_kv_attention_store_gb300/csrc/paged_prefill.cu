@@ -714,6 +714,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         Item it;
         bool ok = true;
         int g = 0;                                      // global key tile
+        // An item's output rows leave its Q buffer through an asynchronous tensor store; the buffer
+        // is handed back to the producer (kBarQEmpty) one step later, once the store has read it.
+        int pend_qb = -1;
+        auto release_stage = [&](int qb) {
+            if (lane == 0)
+                bulk_wait_group_read0();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(BAR(kBarQEmpty + qb));
+        };
         for (int k = 0; ok; ++k) {
             if (!read_item(k, it)) {
                 ok = false;
@@ -786,8 +796,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(BAR(kBarPFull + bb));
                 return true;
             };
-            for (int n = 0; n < it.nkv && ok; ++n, ++g)
+            for (int n = 0; n < it.nkv && ok; ++n, ++g) {
                 ok = n < it.first_masked ? tile(n, std::false_type{}) : tile(n, std::true_type{});
+                if (n == 0 && pend_qb >= 0) {
+                    // the previous item's tensor store has had a step to read its staging buffer
+                    release_stage(pend_qb);
+                    pend_qb = -1;
+                }
+            }
             if (!ok)
                 break;
             // ---- epilogue: O / l -> bf16 rows (before this warpgroup's next P lets PV reuse O) ----
@@ -807,26 +823,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int qb = k % kQBufs;
             const uint32_t stage = base + kOffQ + qb * kTile;
             uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(it.cq0 + tok) * p.num_q_heads + head) * kD);
+            uint32_t o[kD];
 #pragma unroll
-            for (int c = 0; c < kD / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(o_addr + c * 32, v);
-                tmem_wait_ld();
+            for (int c = 0; c < kD / 32; ++c)
+                tmem_ld32(o_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32 * c));
+            tmem_wait_ld();
+            tc_fence_before();      // O reads are ordered before the next item's first PV
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * inv, __uint_as_float(v[8 * j + 1]) * inv);
-                    w.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * inv, __uint_as_float(v[8 * j + 3]) * inv);
-                    w.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * inv, __uint_as_float(v[8 * j + 5]) * inv);
-                    w.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * inv, __uint_as_float(v[8 * j + 7]) * inv);
-                    const int chunk = c * 4 + j;            // 16-byte chunk of the 256-byte row
-                    if (warp_full)
-                        sts_u4(stage + (chunk >> 3) * kHalf + (uint32_t)r * 128u +
-                                   ((uint32_t)((chunk & 7) ^ (r & 7)) << 4),
-                               w);
-                    else if (valid)
-                        dst[chunk] = w;
-                }
+            for (int chunk = 0; chunk < kD / 8; ++chunk) {     // 16-byte chunk of the 256-byte row
+                uint4 w;
+                w.x = pack_bf16x2(__uint_as_float(o[8 * chunk + 0]) * inv, __uint_as_float(o[8 * chunk + 1]) * inv);
+                w.y = pack_bf16x2(__uint_as_float(o[8 * chunk + 2]) * inv, __uint_as_float(o[8 * chunk + 3]) * inv);
+                w.z = pack_bf16x2(__uint_as_float(o[8 * chunk + 4]) * inv, __uint_as_float(o[8 * chunk + 5]) * inv);
+                w.w = pack_bf16x2(__uint_as_float(o[8 * chunk + 6]) * inv, __uint_as_float(o[8 * chunk + 7]) * inv);
+                if (warp_full)
+                    sts_u4(stage + (chunk >> 3) * kHalf + (uint32_t)r * 128u + ((uint32_t)((chunk & 7) ^ (r & 7)) << 4),
+                           w);
+                else if (valid)
+                    dst[chunk] = w;
             }
             if (warp_full) {
                 fence_proxy_async_smem();
@@ -836,14 +850,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int h = 0; h < 2; ++h)
                         tma_store_3d(&tmap_o, stage + h * kHalf + warp * 4096, h * 64, it.kvh * p.group, row0);
                     bulk_commit_group();
-                    bulk_wait_group_read0();
                 }
             }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(BAR(kBarQEmpty + qb));
-            tc_fence_before();      // O reads are ordered before the next item's first PV
+            pend_qb = qb;
         }
+        if (pend_qb >= 0)
+            release_stage(pend_qb);                     // the last store must have read shared memory
         if (!ok && lane == 0)
             flag_error(p.d_err, NV_DERR_TIMEOUT);
     }
