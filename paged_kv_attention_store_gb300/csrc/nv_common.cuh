@@ -193,6 +193,19 @@ __device__ __forceinline__ void bulk_wait_group_read0()
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Warp-specialised register budgets: a whole warpgroup (4 aligned warps) raises or lowers its
+// per-thread register count; the CTA's total must stay within what it was launched with.
+template <int N>
+__device__ __forceinline__ void warpgroup_reg_alloc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void warpgroup_reg_dealloc()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");

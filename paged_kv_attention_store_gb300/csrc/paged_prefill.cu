@@ -59,12 +59,14 @@ constexpr int kQBufs = 2;            // Q buffers: the next item's Q loads while
 constexpr int kKSlots = NVKV_PREFILL_KSLOTS;   // K ring slots
 constexpr int kVSlots = 5 - kKSlots;           // V ring slots
 constexpr int kBufs = 3;             // score / P buffers in TMEM
-#ifndef NVKV_PREFILL_DUAL
-#define NVKV_PREFILL_DUAL 1
-#endif
-// Two MMA-issuing warps (5: S = Q K^T, 6: O += P V) or one (5) that alternates them.
-constexpr bool kDualIssuer = NVKV_PREFILL_DUAL != 0;
-constexpr int kThreads = kDualIssuer ? 224 : 192;    // warps 0-3 softmax; 4 producer; 5 (and 6) MMA
+// Warp roles: 0-3 softmax (warpgroup 0); 4 TMA producer; 5 S = Q K^T issuer (owns TMEM); 6 O += P V
+// issuer; 7-10 epilogue (TMEM lane quarter = warp % 4); 11 idle.  Warpgroup 0 runs with more
+// registers than the others (setmaxnreg); the split must add up to the launch budget.
+constexpr int kThreads = 384;
+constexpr int kWarpProducer = 4, kWarpS = 5, kWarpPV = 6, kWarpEpi0 = 7, kWarpEpiEnd = 11;
+constexpr int kLaunchRegs = 168;                       // per thread at launch (checked on the host)
+constexpr int kSoftmaxRegs = 200, kOtherRegs = 152;
+static_assert(4 * kSoftmaxRegs + 8 * kOtherRegs == 12 * kLaunchRegs, "register split must match the launch");
 constexpr uint32_t kTmemCols = 512;  // buffer b at b*128, O at 384
 constexpr uint32_t kTmemO = 384;
 constexpr float kRescaleLog2 = 8.0f;
@@ -90,12 +92,15 @@ constexpr int kBarPFull = kBarSFull + kBufs;       // + buffer
 constexpr int kBarODone = kBarPFull + kBufs;       // + buffer (PV(n) commits to n % 3; its V slot is free)
 constexpr int kQueue = 8;                          // claimed work items in flight
 constexpr int kItemInts = 12;                      // one work item in the shared-memory queue
-constexpr int kBarItemFull = kBarODone + kBufs;    // + queue slot
+constexpr int kBarOFree = kBarODone + kBufs;       // + item parity: the epilogue has read O (4 warps)
+constexpr int kBarRowSum = kBarOFree + 2;          // + item parity: the softmax has written the row sums
+constexpr int kBarItemFull = kBarRowSum + 2;       // + queue slot
 constexpr int kBarItemEmpty = kBarItemFull + kQueue;
-constexpr int kItemReaders = 6;                    // S cursor, PV cursor, 4 softmax warps
+constexpr int kItemReaders = 2 + 4 + 4;            // S cursor, PV cursor, 4 softmax, 4 epilogue warps
 constexpr int kNumBars = kBarItemEmpty + kQueue;
 constexpr uint32_t kOffItems = kOffBar + kNumBars * 8;
-constexpr uint32_t kOffTmemSlot = kOffItems + kQueue * kItemInts * 4;
+constexpr uint32_t kOffRowSum = kOffItems + kQueue * kItemInts * 4;   // float [2 item parities][128 rows]
+constexpr uint32_t kOffTmemSlot = kOffRowSum + 2 * 128 * 4;
 constexpr uint32_t kSmemBytes = kOffTmemSlot + 16 + 1024;      // + slack for 1024-byte alignment
 static_assert(kSmemBytes <= 227u * 1024u, "shared memory per CTA");
 
@@ -363,6 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(BAR(kBarQFull + s), 1);
             mbar_init(BAR(kBarQEmpty + s), 1 + 4);     // last S of the item + the 4 epilogue warps
+            mbar_init(BAR(kBarOFree + s), 4);
+            mbar_init(BAR(kBarRowSum + s), 4);
         }
         for (int s = 0; s < kKSlots; ++s) {
             mbar_init(BAR(kBarKFull + s), 1);
@@ -404,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(BAR(kBarItemEmpty + k % kQueue));
         return true;
     };
-    if (warp == 5) {
+    if (warp == kWarpS) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
@@ -412,318 +419,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    if (warp == 4) {
-        // =========================== TMA producer ===========================
-        // Copies go out in the order the MMA issuer needs them.  S(j) is issued two key tiles
-        // before PV(j), so K(j) is copied two tiles ahead of V(j): the stream is K(j) V(j-2),
-        // K(j+1) V(j-1), ...  An item's Q tile goes out just before its first K tile (after the
-        // V copy that precedes it: that V feeds the PV whose completion frees the Q buffer).
-        // Lane kb copies box kb of a tile (box_rows keys, both 64-dim halves).
-        const int bs_mask = (1 << p.block_shift) - 1;
-        const int boxes = kBN / p.box_rows;
-        if (lane == 0) {
-            prefetch_tmap(&tmap_q);
-            prefetch_tmap(&tmap_k);
-            prefetch_tmap(&tmap_v);
-            prefetch_tmap(&tmap_o);
-        }
-        struct TileCopy {
-            int slot;           // this lane's box: first pool slot, -1 = none
-            int kvh;
-            uint32_t bytes;     // whole tile
-        };
-        // copy one K or V tile into its ring (idx = its global key tile).  The slot's previous
-        // tile (idx - slots) is free once its MMA group has completed: S for K, PV for V, whose
-        // commits to the score-buffer barriers already signal that.
-        auto copy_tile = [&](bool is_v, int idx, const TileCopy &c) {
-            const int n_slots = is_v ? kVSlots : kKSlots;
-            const int s_ = idx % n_slots;
-            const uint32_t full = BAR((is_v ? kBarVFull : kBarKFull) + s_);
-            const int prev = idx - n_slots;
-            if (prev >= 0 &&
-                !__all_sync(0xffffffffu,
-                            mbar_wait(BAR((is_v ? kBarODone : kBarSFull) + prev % kBufs), (prev / kBufs) & 1)))
-                return false;
-            const uint32_t dst = base + (is_v ? kOffV : kOffK) + s_ * kTile + (uint32_t)lane * p.box_rows * 128u;
-            if (lane == 0)
-                mbar_arrive_expect_tx(full, c.bytes);
-            __syncwarp();
-            if (c.slot >= 0) {
-                const CUtensorMap *map = is_v ? &tmap_v : &tmap_k;
-                tma_load_3d(dst, map, 0, c.kvh, c.slot, full);
-                tma_load_3d(dst + kHalf, map, 64, c.kvh, c.slot, full);
-            }
-            return true;
-        };
-        bool ok = true;
-        int j = 0;                                  // global key tile of the next K copy
-        TileCopy v1{-1, 0, 0}, v2{-1, 0, 0};        // tiles j-1 and j-2, whose V is still to copy
-        // lane 0 claims one item ahead: the counter's answer for item k+1 travels while item k's
-        // copies are issued
-        const int4 *plan = reinterpret_cast<const int4 *>(p.ws + kPlanHeaderInts);
-        int pending = 0;
-        if (lane == 0)
-            pending = atomicAdd(p.ws, 1);
-        for (int k = 0; ok; ++k) {
-            // item k: its claim number, then its work-list entry (lanes 0-1 load the two halves)
-            if (k >= kQueue &&
-                !__all_sync(0xffffffffu, mbar_wait(BAR(kBarItemEmpty + k % kQueue), ((k / kQueue) - 1) & 1))) {
-                ok = false;
-                break;
-            }
-            const int v = __shfl_sync(0xffffffffu, pending, 0);
-            if (lane == 0 && v < total)
-                pending = atomicAdd(p.ws, 1);
-            Item it{};
-            it.v = v < total ? v : total;
-            if (v < total) {
-                const int e = v / p.num_kv_heads;
-                int4 r = make_int4(0, 0, 0, 0);
-                if (lane < 2)
-                    r = plan[2 * e + lane];
-                it.b = __shfl_sync(0xffffffffu, r.x, 0);
-                it.cq0 = __shfl_sync(0xffffffffu, r.y, 0);
-                it.Lq = __shfl_sync(0xffffffffu, r.z, 0);
-                it.P = __shfl_sync(0xffffffffu, r.w, 0);
-                it.i0 = __shfl_sync(0xffffffffu, r.x, 1);
-                it.nq = __shfl_sync(0xffffffffu, r.y, 1);
-                it.kv_len = __shfl_sync(0xffffffffu, r.z, 1);
-                it.nkv = __shfl_sync(0xffffffffu, r.w, 1);
-                it.kvh = v - e * p.num_kv_heads;
-                it.first_masked = (it.P + it.i0 + 1) / kBN;
-            }
-            if (lane == 0) {
-                volatile int *q = items + (k % kQueue) * kItemInts;
-                q[0] = it.v;
-                q[1] = it.b;
-                q[2] = it.kvh;
-                q[3] = it.cq0;
-                q[4] = it.Lq;
-                q[5] = it.P;
-                q[6] = it.i0;
-                q[7] = it.nq;
-                q[8] = it.kv_len;
-                q[9] = it.nkv;
-                q[10] = it.first_masked;
-                mbar_arrive(BAR(kBarItemFull + k % kQueue));
-            }
-            if (v >= total)
-                break;
-            const int32_t *bt = p.block_tables + (size_t)it.b * p.bt_stride;
-            const int nblk = (it.kv_len + (1 << p.block_shift) - 1) >> p.block_shift;
-            int win_base = 0;                       // the block-table row, 32 entries at a time
-            int win = lane < nblk ? __ldg(bt + lane) : -1;
-            for (int n = 0; n < it.nkv && ok; ++n) {
-                // this lane's box of tile n
-                TileCopy cur{-1, it.kvh, 0};
-                const int lb0 = (n * kBN) >> p.block_shift;
-                const int lb_hi = min(lb0 + boxes - 1, nblk - 1);
-                if (lb_hi >= win_base + 32) {       // warp-uniform window move
-                    win_base = lb0;
-                    win = win_base + lane < nblk ? __ldg(bt + win_base + lane) : -1;
-                }
-                const int j0 = n * kBN + lane * p.box_rows;
-                const int lb = j0 >> p.block_shift;
-                const int blk = __shfl_sync(0xffffffffu, win, (lb - win_base) & 31);
-                if (lane < boxes && j0 < it.kv_len) {
-                    if (blk < 0 || blk >= p.num_blocks)
-                        flag_error(p.d_err, NV_DERR_BLOCK_RANGE);
-                    else
-                        cur.slot = (blk << p.block_shift) + (j0 & bs_mask);
-                }
-                cur.bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, cur.slot >= 0)) * p.box_rows * 256u;
-                if (n == 0) {
-                    if (j >= 2 && !copy_tile(true, j - 2, v2)) {
-                        ok = false;
-                        break;
-                    }
-                    // the item's Q, into buffer k % 2 once item k-2's last S and epilogue are done
-                    const int qb = k % kQBufs;
-                    if (k >= kQBufs &&
-                        !__all_sync(0xffffffffu, mbar_wait(BAR(kBarQEmpty + qb), ((k / kQBufs) - 1) & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(BAR(kBarQFull + qb), kTile);
-                        for (int h = 0; h < 2; ++h)
-                            tma_load_3d(base + kOffQ + qb * kTile + h * kHalf, &tmap_q, h * 64,
-                                        it.kvh * p.group, it.cq0 + it.i0, BAR(kBarQFull + qb));
-                    }
-                    if (!copy_tile(false, j, cur)) {
-                        ok = false;
-                        break;
-                    }
-                } else {
-                    if (!copy_tile(false, j, cur) || (j >= 2 && !copy_tile(true, j - 2, v2))) {
-                        ok = false;
-                        break;
-                    }
-                }
-                v2 = v1;
-                v1 = cur;
-                ++j;
-            }
-        }
-        // the last two V tiles
-        if (ok && j >= 2)
-            ok = copy_tile(true, j - 2, v2);
-        if (ok && j >= 1)
-            ok = copy_tile(true, j - 1, v1);
-        if (!ok && lane == 0)
-            flag_error(p.d_err, NV_DERR_TIMEOUT);
-    } else if (warp == 5 || warp == 6) {
-        // ============================ MMA issuer(s) ============================
-        // Key steps of all this CTA's work items form one global sequence g.  S(g) goes to TMEM
-        // buffer g % 3 once PV(g-3) has finished with it; both streams run across tile
-        // boundaries, so the next tile's first scores are computed during the current tile's last
-        // softmax.  (Single-issuer build: the order S(0) S(1) | PV(g) S(g+2) | ...)
-        constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);   // Q, K both K-major
-        constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kD, false, true);     // P (TMEM), V MN-major
-        // Operand descriptors of Q buffer 0 and K / V slot 0; the others differ only in the start
-        // address field (address / 16, 14 bits: every buffer lies below 256 KB), so a buffer's
-        // descriptor is the slot-0 one plus its offset / 16.
-        const uint64_t desc_q0 = smem_desc_sw128(base + kOffQ, 16, 1024);
-        const uint64_t desc_k0 = smem_desc_sw128(base + kOffK, 16, 1024);
-        const uint64_t desc_v0 = smem_desc_sw128(base + kOffV, kHalf, 1024);
-        bool ok = true;
-        auto wait_all = [&](uint32_t b_, uint32_t parity) {
-            ok = ok && __all_sync(0xffffffffu, mbar_wait(b_, parity));
-            return ok;
-        };
-        struct Cursor {
-            Item it;
-            int k;      // work item count
-            int n;      // key tile within the item
-            int g;      // global key tile
-            bool have;  // it holds item k
-        };
-        // true when the cursor has a key tile to issue; reads its item from the queue only when
-        // the cursor reaches it, so the issuer never waits for a claim it does not yet need
-        auto ready = [&](Cursor &c) {
-            if (!c.have) {
-                if (!read_item(c.k, c.it)) {
-                    ok = false;
-                    c.it.v = total;
-                }
-                c.have = true;
-            }
-            return ok && c.it.v < total;
-        };
-        Cursor cs{}, cp{};                           // S cursor, PV cursor
-        auto advance = [&](Cursor &c) {
-            if (++c.n == c.it.nkv) {
-                ++c.k;
-                c.n = 0;
-                c.have = false;
-            }
-            ++c.g;
-        };
-        auto issue_s = [&](Cursor &c) {
-            const int g = c.g;
-            const int slot = g % kKSlots;
-            const int bb = g % kBufs;
-            const int qb = c.k % kQBufs;
-            if (c.n == 0 && !wait_all(BAR(kBarQFull + qb), (c.k / kQBufs) & 1))
-                return;
-            if (!wait_all(BAR(kBarKFull + slot), (g / kKSlots) & 1))
-                return;
-            // buffer bb last held P(g-3): its PV must have finished (one key tile ago)
-            if (g >= kBufs && !wait_all(BAR(kBarODone + bb), ((g - kBufs) / kBufs) & 1))
-                return;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint64_t dq = desc_q0 + (uint64_t)(qb * (kTile >> 4));
-                const uint64_t dk = desc_k0 + (uint64_t)(slot * (kTile >> 4));
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    // k-step kk: 16 dims = 32 bytes into the 128-byte swizzle row, 64 dims per half
-                    const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
-                    mma_bf16_ss(tmem + bb * 128, dq + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(BAR(kBarSFull + bb));
-                if (c.n == c.it.nkv - 1)
-                    mma_commit(BAR(kBarQEmpty + qb));   // the item's last use of its Q buffer
-            }
-            __syncwarp();
-            advance(c);
-        };
-        auto issue_pv = [&](Cursor &c) {
-            const int g = c.g;
-            const int n = c.n;
-            const int slot = g % kVSlots;
-            const int bb = g % kBufs;
-            if (!wait_all(BAR(kBarVFull + slot), (g / kVSlots) & 1))
-                return;
-            const uint32_t vtile = base + kOffV + slot * kTile;
-            // Keys past the sequence carry P = 0, but their V rows may hold anything (NaN patterns
-            // included) and 0 * NaN would poison O: zero them.  (Skipping their k-steps instead
-            // measured slower.)
-            const int vrows = min(c.it.kv_len - n * kBN, kBN);
-            if (vrows < kBN) {
-                for (int c2 = lane; c2 < (kBN - vrows) * 16; c2 += 32)     // 16-byte chunk: row, half, column
-                    sts_u4(vtile + ((c2 >> 3) & 1) * kHalf + (uint32_t)(vrows + (c2 >> 4)) * 128u +
-                               (uint32_t)(c2 & 7) * 16u,
-                           make_uint4(0, 0, 0, 0));
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            if (!wait_all(BAR(kBarPFull + bb), (g / kBufs) & 1))
-                return;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint64_t dv = desc_v0 + (uint64_t)(slot * (kTile >> 4));
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)      // k-step kk: keys 16kk.. = 16 rows of 128 bytes
-                    mma_bf16_ts(tmem + kTmemO, tmem + bb * 128 + kk * 8, dv + (uint64_t)(kk * 16 * 128 >> 4),
-                                idesc_o, (n > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(BAR(kBarODone + bb));
-            }
-            __syncwarp();
-            advance(c);
-        };
-        if (kDualIssuer) {
-            // each warp streams its own groups; S(g) goes as soon as PV(g-3) has freed its buffer
-            if (warp == 5) {
-                while (ready(cs))
-                    issue_s(cs);
-            } else {
-                while (ready(cp))
-                    issue_pv(cp);
-            }
-        } else {
-            // S runs two key tiles ahead of PV
-            if (ready(cs))
-                issue_s(cs);
-            if (ready(cs))
-                issue_s(cs);
-            while (ready(cp)) {
-                issue_pv(cp);
-                if (ready(cs))
-                    issue_s(cs);
-            }
-        }
-        if (!ok && lane == 0)
-            flag_error(p.d_err, NV_DERR_TIMEOUT);
-    } else {
-        // ================= softmax / correction / epilogue (warps 0-3) =================
+    if (warp < 4) {
+        warpgroup_reg_alloc<kSoftmaxRegs>();
+        // ======================= softmax / correction (warps 0-3) =======================
         const int r = threadIdx.x;                      // tile row == TMEM lane
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const uint32_t o_addr = tmem + lane_base + kTmemO;
+        volatile float *rowsum = reinterpret_cast<volatile float *>(smem + kOffRowSum);
         Item it;
         bool ok = true;
         int g = 0;                                      // global key tile
-        // An item's output rows leave its Q buffer through an asynchronous tensor store; the buffer
-        // is handed back to the producer (kBarQEmpty) one step later, once the store has read it.
-        int pend_qb = -1;
-        auto release_stage = [&](int qb) {
-            if (lane == 0)
-                bulk_wait_group_read0();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(BAR(kBarQEmpty + qb));
-        };
         for (int k = 0; ok; ++k) {
             if (!read_item(k, it)) {
                 ok = false;
@@ -732,8 +437,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (it.v >= total)
                 break;
             const int tok = it.i0 + (r >> p.group_shift);   // token index inside the chunk
-            const int head = it.kvh * p.group + (r & (p.group - 1));
-            const bool valid = tok < it.Lq;
             const int lim = it.P + tok;                 // last key this row may see
             float m_run = -INFINITY;                    // running max of scale*log2(e)*s
             float l_run = 0.f;
@@ -796,74 +499,396 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(BAR(kBarPFull + bb));
                 return true;
             };
-            for (int n = 0; n < it.nkv && ok; ++n, ++g) {
+            for (int n = 0; n < it.nkv && ok; ++n, ++g)
                 ok = n < it.first_masked ? tile(n, std::false_type{}) : tile(n, std::true_type{});
-                if (n == 0 && pend_qb >= 0) {
-                    // the previous item's tensor store has had a step to read its staging buffer
-                    release_stage(pend_qb);
-                    pend_qb = -1;
-                }
-            }
             if (!ok)
                 break;
-            // ---- epilogue: O / l -> bf16 rows (before this warpgroup's next P lets PV reuse O) ----
-            // The last PV's completion also means every S of the item has read its Q buffer, so
-            // the rows are staged there (same 128-byte swizzled layout as the Q tile: row r of
-            // the tile is TMEM lane r) and each warp writes its 32 rows with one tensor store per
-            // 64-dim half.  A warp whose rows run past the chunk's end (the ragged last tile)
-            // stores its valid rows directly instead, so it never touches the next sequence.
-            const int last = g - 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(BAR(kBarODone + last % kBufs), (last / kBufs) & 1))) {
+            // Hand the row sums to the epilogue warps and go on with the next item at once.  The
+            // sums of item k share a buffer with item k-2's, which that epilogue must have read.
+            if (k >= 2 && !__all_sync(0xffffffffu, mbar_wait(BAR(kBarOFree + (k & 1)), ((k - 2) >> 1) & 1))) {
                 ok = false;
                 break;
             }
-            tc_fence_after();
-            const float inv = (valid && l_run > 0.f) ? 1.f / l_run : 0.f;
-            const bool warp_full = __all_sync(0xffffffffu, valid);
-            const int qb = k % kQBufs;
-            const uint32_t stage = base + kOffQ + qb * kTile;
-            uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(it.cq0 + tok) * p.num_q_heads + head) * kD);
-            uint32_t o[kD];
-#pragma unroll
-            for (int c = 0; c < kD / 32; ++c)
-                tmem_ld32(o_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32 * c));
-            tmem_wait_ld();
-            tc_fence_before();      // O reads are ordered before the next item's first PV
-#pragma unroll
-            for (int chunk = 0; chunk < kD / 8; ++chunk) {     // 16-byte chunk of the 256-byte row
-                uint4 w;
-                w.x = pack_bf16x2(__uint_as_float(o[8 * chunk + 0]) * inv, __uint_as_float(o[8 * chunk + 1]) * inv);
-                w.y = pack_bf16x2(__uint_as_float(o[8 * chunk + 2]) * inv, __uint_as_float(o[8 * chunk + 3]) * inv);
-                w.z = pack_bf16x2(__uint_as_float(o[8 * chunk + 4]) * inv, __uint_as_float(o[8 * chunk + 5]) * inv);
-                w.w = pack_bf16x2(__uint_as_float(o[8 * chunk + 6]) * inv, __uint_as_float(o[8 * chunk + 7]) * inv);
-                if (warp_full)
-                    sts_u4(stage + (chunk >> 3) * kHalf + (uint32_t)r * 128u + ((uint32_t)((chunk & 7) ^ (r & 7)) << 4),
-                           w);
-                else if (valid)
-                    dst[chunk] = w;
-            }
-            if (warp_full) {
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const int row0 = it.cq0 + it.i0 + ((warp * 32) >> p.group_shift);
-                    for (int h = 0; h < 2; ++h)
-                        tma_store_3d(&tmap_o, stage + h * kHalf + warp * 4096, h * 64, it.kvh * p.group, row0);
-                    bulk_commit_group();
-                }
-            }
-            pend_qb = qb;
+            rowsum[(k & 1) * 128 + r] = l_run;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(BAR(kBarRowSum + (k & 1)));
         }
-        if (pend_qb >= 0)
-            release_stage(pend_qb);                     // the last store must have read shared memory
         if (!ok && lane == 0)
             flag_error(p.d_err, NV_DERR_TIMEOUT);
+    } else {
+        warpgroup_reg_dealloc<kOtherRegs>();
+        if (warp == kWarpProducer) {
+            // =========================== TMA producer ===========================
+            // Copies go out in the order the MMA issuer needs them.  S(j) is issued two key tiles
+            // before PV(j), so K(j) is copied two tiles ahead of V(j): the stream is K(j) V(j-2),
+            // K(j+1) V(j-1), ...  An item's Q tile goes out just before its first K tile (after the
+            // V copy that precedes it: that V feeds the PV whose completion frees the Q buffer).
+            // Lane kb copies box kb of a tile (box_rows keys, both 64-dim halves).
+            const int bs_mask = (1 << p.block_shift) - 1;
+            const int boxes = kBN / p.box_rows;
+            if (lane == 0) {
+                prefetch_tmap(&tmap_q);
+                prefetch_tmap(&tmap_k);
+                prefetch_tmap(&tmap_v);
+                prefetch_tmap(&tmap_o);
+            }
+            struct TileCopy {
+                int slot;           // this lane's box: first pool slot, -1 = none
+                int kvh;
+                uint32_t bytes;     // whole tile
+            };
+            // copy one K or V tile into its ring (idx = its global key tile).  The slot's previous
+            // tile (idx - slots) is free once its MMA group has completed: S for K, PV for V, whose
+            // commits to the score-buffer barriers already signal that.
+            auto copy_tile = [&](bool is_v, int idx, const TileCopy &c) {
+                const int n_slots = is_v ? kVSlots : kKSlots;
+                const int s_ = idx % n_slots;
+                const uint32_t full = BAR((is_v ? kBarVFull : kBarKFull) + s_);
+                const int prev = idx - n_slots;
+                if (prev >= 0 &&
+                    !__all_sync(0xffffffffu,
+                                mbar_wait(BAR((is_v ? kBarODone : kBarSFull) + prev % kBufs), (prev / kBufs) & 1)))
+                    return false;
+                const uint32_t dst = base + (is_v ? kOffV : kOffK) + s_ * kTile + (uint32_t)lane * p.box_rows * 128u;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(full, c.bytes);
+                __syncwarp();
+                if (c.slot >= 0) {
+                    const CUtensorMap *map = is_v ? &tmap_v : &tmap_k;
+                    tma_load_3d(dst, map, 0, c.kvh, c.slot, full);
+                    tma_load_3d(dst + kHalf, map, 64, c.kvh, c.slot, full);
+                }
+                return true;
+            };
+            bool ok = true;
+            int j = 0;                                  // global key tile of the next K copy
+            TileCopy v1{-1, 0, 0}, v2{-1, 0, 0};        // tiles j-1 and j-2, whose V is still to copy
+            // lane 0 claims one item ahead: the counter's answer for item k+1 travels while item k's
+            // copies are issued
+            const int4 *plan = reinterpret_cast<const int4 *>(p.ws + kPlanHeaderInts);
+            int pending = 0;
+            if (lane == 0)
+                pending = atomicAdd(p.ws, 1);
+            for (int k = 0; ok; ++k) {
+                // item k: its claim number, then its work-list entry (lanes 0-1 load the two halves)
+                if (k >= kQueue &&
+                    !__all_sync(0xffffffffu, mbar_wait(BAR(kBarItemEmpty + k % kQueue), ((k / kQueue) - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                const int v = __shfl_sync(0xffffffffu, pending, 0);
+                if (lane == 0 && v < total)
+                    pending = atomicAdd(p.ws, 1);
+                Item it{};
+                it.v = v < total ? v : total;
+                if (v < total) {
+                    const int e = v / p.num_kv_heads;
+                    int4 r = make_int4(0, 0, 0, 0);
+                    if (lane < 2)
+                        r = plan[2 * e + lane];
+                    it.b = __shfl_sync(0xffffffffu, r.x, 0);
+                    it.cq0 = __shfl_sync(0xffffffffu, r.y, 0);
+                    it.Lq = __shfl_sync(0xffffffffu, r.z, 0);
+                    it.P = __shfl_sync(0xffffffffu, r.w, 0);
+                    it.i0 = __shfl_sync(0xffffffffu, r.x, 1);
+                    it.nq = __shfl_sync(0xffffffffu, r.y, 1);
+                    it.kv_len = __shfl_sync(0xffffffffu, r.z, 1);
+                    it.nkv = __shfl_sync(0xffffffffu, r.w, 1);
+                    it.kvh = v - e * p.num_kv_heads;
+                    it.first_masked = (it.P + it.i0 + 1) / kBN;
+                }
+                if (lane == 0) {
+                    volatile int *q = items + (k % kQueue) * kItemInts;
+                    q[0] = it.v;
+                    q[1] = it.b;
+                    q[2] = it.kvh;
+                    q[3] = it.cq0;
+                    q[4] = it.Lq;
+                    q[5] = it.P;
+                    q[6] = it.i0;
+                    q[7] = it.nq;
+                    q[8] = it.kv_len;
+                    q[9] = it.nkv;
+                    q[10] = it.first_masked;
+                    mbar_arrive(BAR(kBarItemFull + k % kQueue));
+                }
+                if (v >= total)
+                    break;
+                const int32_t *bt = p.block_tables + (size_t)it.b * p.bt_stride;
+                const int nblk = (it.kv_len + (1 << p.block_shift) - 1) >> p.block_shift;
+                int win_base = 0;                       // the block-table row, 32 entries at a time
+                int win = lane < nblk ? __ldg(bt + lane) : -1;
+                for (int n = 0; n < it.nkv && ok; ++n) {
+                    // this lane's box of tile n
+                    TileCopy cur{-1, it.kvh, 0};
+                    const int lb0 = (n * kBN) >> p.block_shift;
+                    const int lb_hi = min(lb0 + boxes - 1, nblk - 1);
+                    if (lb_hi >= win_base + 32) {       // warp-uniform window move
+                        win_base = lb0;
+                        win = win_base + lane < nblk ? __ldg(bt + win_base + lane) : -1;
+                    }
+                    const int j0 = n * kBN + lane * p.box_rows;
+                    const int lb = j0 >> p.block_shift;
+                    const int blk = __shfl_sync(0xffffffffu, win, (lb - win_base) & 31);
+                    if (lane < boxes && j0 < it.kv_len) {
+                        if (blk < 0 || blk >= p.num_blocks)
+                            flag_error(p.d_err, NV_DERR_BLOCK_RANGE);
+                        else
+                            cur.slot = (blk << p.block_shift) + (j0 & bs_mask);
+                    }
+                    cur.bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, cur.slot >= 0)) * p.box_rows * 256u;
+                    if (n == 0) {
+                        if (j >= 2 && !copy_tile(true, j - 2, v2)) {
+                            ok = false;
+                            break;
+                        }
+                        // the item's Q, into buffer k % 2 once item k-2's last S and epilogue are done
+                        const int qb = k % kQBufs;
+                        if (k >= kQBufs &&
+                            !__all_sync(0xffffffffu, mbar_wait(BAR(kBarQEmpty + qb), ((k / kQBufs) - 1) & 1))) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(BAR(kBarQFull + qb), kTile);
+                            for (int h = 0; h < 2; ++h)
+                                tma_load_3d(base + kOffQ + qb * kTile + h * kHalf, &tmap_q, h * 64,
+                                            it.kvh * p.group, it.cq0 + it.i0, BAR(kBarQFull + qb));
+                        }
+                        if (!copy_tile(false, j, cur)) {
+                            ok = false;
+                            break;
+                        }
+                    } else {
+                        if (!copy_tile(false, j, cur) || (j >= 2 && !copy_tile(true, j - 2, v2))) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    v2 = v1;
+                    v1 = cur;
+                    ++j;
+                }
+            }
+            // the last two V tiles
+            if (ok && j >= 2)
+                ok = copy_tile(true, j - 2, v2);
+            if (ok && j >= 1)
+                ok = copy_tile(true, j - 1, v1);
+            if (!ok && lane == 0)
+                flag_error(p.d_err, NV_DERR_TIMEOUT);
+        } else if (warp == kWarpS || warp == kWarpPV) {
+            // ============================ MMA issuer(s) ============================
+            // Key steps of all this CTA's work items form one global sequence g.  S(g) goes to TMEM
+            // buffer g % 3 once PV(g-3) has finished with it; both streams run across tile
+            // boundaries, so the next tile's first scores are computed during the current tile's last
+            // softmax.  (Single-issuer build: the order S(0) S(1) | PV(g) S(g+2) | ...)
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);   // Q, K both K-major
+            constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kD, false, true);     // P (TMEM), V MN-major
+            // Operand descriptors of Q buffer 0 and K / V slot 0; the others differ only in the start
+            // address field (address / 16, 14 bits: every buffer lies below 256 KB), so a buffer's
+            // descriptor is the slot-0 one plus its offset / 16.
+            const uint64_t desc_q0 = smem_desc_sw128(base + kOffQ, 16, 1024);
+            const uint64_t desc_k0 = smem_desc_sw128(base + kOffK, 16, 1024);
+            const uint64_t desc_v0 = smem_desc_sw128(base + kOffV, kHalf, 1024);
+            bool ok = true;
+            auto wait_all = [&](uint32_t b_, uint32_t parity) {
+                ok = ok && __all_sync(0xffffffffu, mbar_wait(b_, parity));
+                return ok;
+            };
+            struct Cursor {
+                Item it;
+                int k;      // work item count
+                int n;      // key tile within the item
+                int g;      // global key tile
+                bool have;  // it holds item k
+            };
+            // true when the cursor has a key tile to issue; reads its item from the queue only when
+            // the cursor reaches it, so the issuer never waits for a claim it does not yet need
+            auto ready = [&](Cursor &c) {
+                if (!c.have) {
+                    if (!read_item(c.k, c.it)) {
+                        ok = false;
+                        c.it.v = total;
+                    }
+                    c.have = true;
+                }
+                return ok && c.it.v < total;
+            };
+            Cursor cs{}, cp{};                           // S cursor, PV cursor
+            auto advance = [&](Cursor &c) {
+                if (++c.n == c.it.nkv) {
+                    ++c.k;
+                    c.n = 0;
+                    c.have = false;
+                }
+                ++c.g;
+            };
+            auto issue_s = [&](Cursor &c) {
+                const int g = c.g;
+                const int slot = g % kKSlots;
+                const int bb = g % kBufs;
+                const int qb = c.k % kQBufs;
+                if (c.n == 0 && !wait_all(BAR(kBarQFull + qb), (c.k / kQBufs) & 1))
+                    return;
+                if (!wait_all(BAR(kBarKFull + slot), (g / kKSlots) & 1))
+                    return;
+                // buffer bb last held P(g-3): its PV must have finished (one key tile ago)
+                if (g >= kBufs && !wait_all(BAR(kBarODone + bb), ((g - kBufs) / kBufs) & 1))
+                    return;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t dq = desc_q0 + (uint64_t)(qb * (kTile >> 4));
+                    const uint64_t dk = desc_k0 + (uint64_t)(slot * (kTile >> 4));
+    #pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        // k-step kk: 16 dims = 32 bytes into the 128-byte swizzle row, 64 dims per half
+                        const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+                        mma_bf16_ss(tmem + bb * 128, dq + off, dk + off, idesc_s, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(BAR(kBarSFull + bb));
+                    if (c.n == c.it.nkv - 1)
+                        mma_commit(BAR(kBarQEmpty + qb));   // the item's last use of its Q buffer
+                }
+                __syncwarp();
+                advance(c);
+            };
+            auto issue_pv = [&](Cursor &c) {
+                const int g = c.g;
+                const int n = c.n;
+                const int slot = g % kVSlots;
+                const int bb = g % kBufs;
+                if (!wait_all(BAR(kBarVFull + slot), (g / kVSlots) & 1))
+                    return;
+                const uint32_t vtile = base + kOffV + slot * kTile;
+                // Keys past the sequence carry P = 0, but their V rows may hold anything (NaN patterns
+                // included) and 0 * NaN would poison O: zero them.  (Skipping their k-steps instead
+                // measured slower.)
+                const int vrows = min(c.it.kv_len - n * kBN, kBN);
+                if (vrows < kBN) {
+                    for (int c2 = lane; c2 < (kBN - vrows) * 16; c2 += 32)     // 16-byte chunk: row, half, column
+                        sts_u4(vtile + ((c2 >> 3) & 1) * kHalf + (uint32_t)(vrows + (c2 >> 4)) * 128u +
+                                   (uint32_t)(c2 & 7) * 16u,
+                               make_uint4(0, 0, 0, 0));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (!wait_all(BAR(kBarPFull + bb), (g / kBufs) & 1))
+                    return;
+                // an item's first PV overwrites O: the previous item's epilogue must have read it
+                if (n == 0 && c.k > 0 && !wait_all(BAR(kBarOFree + ((c.k - 1) & 1)), ((c.k - 1) >> 1) & 1))
+                    return;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t dv = desc_v0 + (uint64_t)(slot * (kTile >> 4));
+    #pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)      // k-step kk: keys 16kk.. = 16 rows of 128 bytes
+                        mma_bf16_ts(tmem + kTmemO, tmem + bb * 128 + kk * 8, dv + (uint64_t)(kk * 16 * 128 >> 4),
+                                    idesc_o, (n > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(BAR(kBarODone + bb));
+                }
+                __syncwarp();
+                advance(c);
+            };
+            // each warp streams its own groups; S(g) goes as soon as PV(g-3) has freed its buffer
+            if (warp == kWarpS) {
+                while (ready(cs))
+                    issue_s(cs);
+            } else {
+                while (ready(cp))
+                    issue_pv(cp);
+            }
+            if (!ok && lane == 0)
+                flag_error(p.d_err, NV_DERR_TIMEOUT);
+        } else if (warp >= kWarpEpi0 && warp < kWarpEpiEnd) {
+            // ============================ epilogue (warps 7-10) ============================
+            // Item by item: wait for the softmax's row sums and the item's last PV, read O from TMEM
+            // (then the next item's PVs may overwrite it), normalise, round to bf16, stage the rows in
+            // the item's Q buffer (every S of the item has read it by then; same 128-byte swizzled
+            // layout as the Q tile, row r = TMEM lane r) and write each warp's 32 rows with one tensor
+            // store per 64-dim half.  A warp whose rows run past the chunk's end (the ragged last tile)
+            // stores its valid rows directly instead, so it never touches the next sequence.
+            const int r = (warp & 3) * 32 + lane;           // tile row == TMEM lane
+            const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+            const uint32_t o_addr = tmem + lane_base + kTmemO;
+            const volatile float *rowsum = reinterpret_cast<const volatile float *>(smem + kOffRowSum);
+            Item it;
+            bool ok = true;
+            int g = 0;                                      // global key step
+            for (int k = 0; ok; ++k) {
+                if (!read_item(k, it)) {
+                    ok = false;
+                    break;
+                }
+                if (it.v >= total)
+                    break;
+                g += it.nkv;
+                const int last = g - 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(BAR(kBarRowSum + (k & 1)), (k >> 1) & 1)) ||
+                    !__all_sync(0xffffffffu, mbar_wait(BAR(kBarODone + last % kBufs), (last / kBufs) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int tok = it.i0 + (r >> p.group_shift);
+                const int head = it.kvh * p.group + (r & (p.group - 1));
+                const bool valid = tok < it.Lq;
+                const float l_row = rowsum[(k & 1) * 128 + r];
+                const float inv = (valid && l_row > 0.f) ? 1.f / l_row : 0.f;
+                // O -> registers as bf16 pairs, 32 columns at a time
+                uint32_t ob[kD / 2];
+#pragma unroll
+                for (int c = 0; c < kD / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(o_addr + c * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        ob[c * 16 + j] = pack_bf16x2(__uint_as_float(v[2 * j]) * inv, __uint_as_float(v[2 * j + 1]) * inv);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(BAR(kBarOFree + (k & 1)));  // O and this item's row sums are read
+                const bool warp_full = __all_sync(0xffffffffu, valid);
+                const int qb = k % kQBufs;
+                const uint32_t stage = base + kOffQ + qb * kTile;
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out + ((size_t)(it.cq0 + tok) * p.num_q_heads + head) * kD);
+#pragma unroll
+                for (int chunk = 0; chunk < kD / 8; ++chunk) {     // 16-byte chunk of the 256-byte row
+                    const uint4 w = make_uint4(ob[4 * chunk], ob[4 * chunk + 1], ob[4 * chunk + 2], ob[4 * chunk + 3]);
+                    if (warp_full)
+                        sts_u4(stage + (chunk >> 3) * kHalf + (uint32_t)r * 128u +
+                                   ((uint32_t)((chunk & 7) ^ (r & 7)) << 4),
+                               w);
+                    else if (valid)
+                        dst[chunk] = w;
+                }
+                if (warp_full) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int row0 = it.cq0 + it.i0 + (((warp & 3) * 32) >> p.group_shift);
+                        for (int h = 0; h < 2; ++h)
+                            tma_store_3d(&tmap_o, stage + h * kHalf + (warp & 3) * 4096, h * 64, it.kvh * p.group, row0);
+                        bulk_commit_group();
+                        bulk_wait_group_read0();            // the staging buffer goes back to the producer
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(BAR(kBarQEmpty + qb));
+            }
+            if (!ok && lane == 0)
+                flag_error(p.d_err, NV_DERR_TIMEOUT);
+        }
     }
 
     // ---------------- teardown: every TMEM access is done before the free ----------------
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpS) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -1017,11 +1042,21 @@ extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const v
         return NV_ERR_CUDA;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
+    static bool regs_ok = false;
     std::call_once(attr_once, [] {
         attr_err = cudaFuncSetAttribute(paged_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        // the warpgroups' register split (setmaxnreg) adds up to exactly the launch budget: refuse to
+        // launch a build whose per-thread register count differs, rather than let a warpgroup wait
+        // for registers that never come
+        cudaFuncAttributes fa{};
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncGetAttributes(&fa, paged_prefill_kernel);
+        regs_ok = attr_err == cudaSuccess && fa.numRegs == kLaunchRegs;
     });
     if (attr_err != cudaSuccess)
         return NV_ERR_CUDA;
+    if (!regs_ok)
+        return NV_ERR_UNSUPPORTED;
     prefill_plan_kernel<<<1, kPlanThreads, 0, (cudaStream_t)stream>>>(pp);
     // persistent: one CTA per SM (shared memory and TMEM admit one); CTAs claim the work list's
     // entries heaviest first
