@@ -288,6 +288,23 @@ def run_ours(args, rank, world, local_rank):
         barrier()
         e2e_ms = e0.elapsed_time(e1)
 
+        # fused store + decode (one pass, nv_store_decode_attn) on the same batch
+        def fused_step():
+            nv.nv_store_decode_attn(q, k_new, v_new, slots, k_cache, v_cache, bt, ctx, db.scale, out=out,
+                                    max_context_len=maxc, workspace=ws, d_err=d_err)
+
+        for _ in range(args.warmup):
+            fused_step()
+        barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            fused_step()
+        f1.record(stream)
+        barrier()
+        fused_ms = f0.elapsed_time(f1)
+        assert int(d_err.item()) == 0, f"device error flags {int(d_err.item())}"
+
         # ---------------- prefill phase: store + prefill on the chunked-prefill batch ----------------
         del k_cache, v_cache, ws
         torch.cuda.empty_cache()
@@ -333,6 +350,7 @@ def run_ours(args, rank, world, local_rank):
     dec_ms_max = max_over_ranks(dec_ms)
     e2e_ms_max = max_over_ranks(e2e_ms)
     dec_kernel_ms_max = max_over_ranks(dec_kernel_ms)
+    fused_ms_max = max_over_ranks(fused_ms)
     pf_ms_max = max_over_ranks(pf_ms)
     pf_step_ms_max = max_over_ranks(pf_step_ms)
     store_ms_max = max_over_ranks(store_ms)
@@ -391,9 +409,17 @@ def run_ours(args, rank, world, local_rank):
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max / args.steps, 4)},
-        "gpu_launches": (launches_per_decode_step * 2 + 3) * args.steps,
-        "gpu_launches_note": "decode phase: store + split-KV decode + merge per step; "
-                             "e2e phase: same kernels; prefill phase: store + work-list pre-pass + prefill per step",
+        "fused_store_decode": {
+            "kernel": "paged_decode_kernel<4, 8, fused> + merge_splits_kernel (nv_store_decode_attn)",
+            "value": round(kv_total / (fused_ms_max * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(fused_ms_max / args.steps, 4),
+            "separate_ms_per_step": round(dec_ms_max / args.steps, 4),
+            "note": "same step as the headline (store 512 rows + decode) in one pass: the new rows are read once "
+                    "from the inputs and written to the pool by the decode kernel",
+        },
+        "gpu_launches": (launches_per_decode_step * 2 + (launches_per_decode_step - 1) + 3) * args.steps,
+        "gpu_launches_note": "decode phase: store + split-KV decode + merge per step; e2e phase: same kernels; "
+                             "fused phase: fused decode + merge; prefill phase: store + work-list pre-pass + prefill",
         "clocks": clocks,
         "prefill": {
             "workload": "chunked prefill with prefix cache (store 16384 new rows + causal varlen prefill): 16 seqs, "

@@ -60,6 +60,7 @@ typedef enum nv_status {
 #define NV_DERR_BLOCK_RANGE 0x2   /* a needed block-table entry outside [0, num_blocks): its keys skipped */
 #define NV_DERR_LENGTH 0x4        /* a length exceeds the block table, the host hint, or is negative */
 #define NV_DERR_TIMEOUT 0x8       /* a bounded wait on an asynchronous copy gave up */
+#define NV_DERR_SLOT_MISMATCH 0x10 /* fused store + decode: a slot that is not position L-1's (row not stored) */
 
 /* Human-readable name of an nv_status value (static string). */
 const char *nv_status_string(int status);
@@ -123,6 +124,38 @@ int nv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache
                          int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
                          void *out, void *workspace, size_t workspace_bytes, int32_t *d_err,
                          nv_stream_t stream);
+
+/*
+ * nv_store_decode_attn -- nv_store_kvcache followed by nv_paged_decode_attn, in one pass.
+ *
+ * Field guide Step 10.3: every decode forward first stores the new token's K/V (store kernel) and
+ * then attends over the history that now ends with it (decode branch); Step 07.6: the new token
+ * is position context_lens[b]-1 of sequence b, and its slot is slot_mapping[b].  This call does
+ * both with the same kernels as the decode: the new rows are read once from k / v, used as
+ * position L-1, and written to their slot by the CTA that attends over that position, so the
+ * store costs no launch and no re-read from the pool.
+ *
+ *   q, block_tables, context_lens, out, workspace, scale, max_context_len: as nv_paged_decode_attn
+ *                 (same workspace size).
+ *   k, v          bf16 [num_seqs, num_kv_heads, head_dim], one new row per sequence; heads
+ *                 contiguous, rows k_row_stride / v_row_stride elements apart (>= Hkv*head_dim,
+ *                 multiples of 8), base pointers 16-byte aligned.
+ *   slot_mapping  int32 [num_seqs]: -1 = no new row for this sequence (graph padding; position
+ *                 L-1, if any, is then read from the pool).  A slot >= 0 must be the slot of
+ *                 position L-1 through block_tables[b] (as the engine builds it); any other slot is
+ *                 not written, position L-1 is read from the pool, and NV_DERR_SLOT_MISMATCH is set
+ *                 (NV_DERR_SLOT_RANGE when it lies outside the pool).
+ * The result (cache and out) equals nv_store_kvcache then nv_paged_decode_attn with the same
+ * arguments whenever the slots follow that rule.  The new slots must not lie in another
+ * sequence's history within the same call (they never do: a new token's slot belongs to its
+ * own sequence).
+ */
+int nv_store_decode_attn(const void *q, const void *k, int64_t k_row_stride, const void *v, int64_t v_row_stride,
+                         const int32_t *slot_mapping, void *k_cache, void *v_cache, const int32_t *block_tables,
+                         int32_t bt_stride, const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                         int32_t max_context_len, float scale, void *out, void *workspace, size_t workspace_bytes,
+                         int32_t *d_err, nv_stream_t stream);
 
 /*
  * nv_paged_decode_attn_noalloc -- nv_paged_decode_attn without a caller-provided workspace.

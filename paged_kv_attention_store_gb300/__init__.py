@@ -27,9 +27,11 @@ NV_DERR_SLOT_RANGE = 0x1
 NV_DERR_BLOCK_RANGE = 0x2
 NV_DERR_LENGTH = 0x4
 NV_DERR_TIMEOUT = 0x8
+NV_DERR_SLOT_MISMATCH = 0x10
 
 EXPORTED = ("nv_status_string", "nv_store_kvcache", "nv_paged_decode_workspace_size", "nv_paged_decode_attn",
-            "nv_paged_decode_attn_noalloc", "nv_paged_prefill_workspace_size", "nv_paged_prefill_attn")
+            "nv_store_decode_attn", "nv_paged_decode_attn_noalloc", "nv_paged_prefill_workspace_size",
+            "nv_paged_prefill_attn")
 
 
 class NvError(RuntimeError):
@@ -63,6 +65,9 @@ def load_library(path: str | None = None):
     L.nv_paged_decode_workspace_size.restype = sz
     L.nv_paged_decode_attn.argtypes = [V, V, V, V, i32, V, i32, i32, i32, i32, i32, i32, i32, f32, V, V, sz, V, V]
     L.nv_paged_decode_attn.restype = ctypes.c_int
+    L.nv_store_decode_attn.argtypes = [V, V, i64, V, i64, V, V, V, V, i32, V, i32, i32, i32, i32, i32, i32, i32, f32,
+                                       V, V, sz, V, V]
+    L.nv_store_decode_attn.restype = ctypes.c_int
     L.nv_paged_decode_attn_noalloc.argtypes = [V, V, V, V, i32, V, i32, i32, i32, i32, i32, i32, i32, f32, V, V, V]
     L.nv_paged_decode_attn_noalloc.restype = ctypes.c_int
     L.nv_paged_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32]
@@ -147,6 +152,37 @@ def nv_paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale,
         hkv, d, bs, nb, int(max_context_len), float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_err),
         _stream(stream))
     _check("nv_paged_decode_attn", rc)
+    return out
+
+
+def nv_store_decode_attn(q, k, v, slot_mapping, k_cache, v_cache, block_tables, context_lens, scale, out=None,
+                         max_context_len=None, workspace=None, d_err=None, stream=None):
+    """Store each sequence's new K/V row (``k``/``v`` ``[B, Hkv, D]`` at ``slot_mapping``) and run decode
+    attention over the history that ends with it, in one pass (same result as ``nv_store_kvcache``
+    then ``nv_paged_decode_attn``).  ``workspace`` as for ``nv_paged_decode_attn``."""
+    import torch
+    nb, bs, hkv, d = _pool_shape(k_cache, v_cache)
+    B, hq, dq = (int(x) for x in q.shape)
+    _need(dq == d and q.is_contiguous(), "q must be contiguous [B, Hq, D]")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == B and block_tables.stride(1) == 1,
+          "block_tables must be [B, W] with unit column stride")
+    _need(int(slot_mapping.shape[0]) == B, "slot_mapping must have one entry per sequence")
+    for name, t in (("k", k), ("v", v)):
+        _need(t.dim() == 3 and tuple(t.shape) == (B, hkv, d), f"{name} must be [B, Hkv, D] = {(B, hkv, d)}")
+        _need(t.stride(2) == 1 and t.stride(1) == d, f"{name} heads must be contiguous")
+    if max_context_len is None:
+        max_context_len = int(block_tables.shape[1]) * bs
+    if out is None:
+        out = torch.empty_like(q)
+    ws_need = nv_paged_decode_workspace_size(B, hq, d, int(max_context_len))
+    if workspace is None and ws_need:
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().nv_store_decode_attn(
+        _ptr(q), _ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), block_tables.stride(0), _ptr(context_lens), B, hq, hkv, d, bs, nb, int(max_context_len),
+        float(scale), _ptr(out), _ptr(workspace), ws_bytes, _ptr(d_err), _stream(stream))
+    _check("nv_store_decode_attn", rc)
     return out
 
 

@@ -24,6 +24,9 @@
 //   * A sequence split over several CTAs writes unnormalised partial outputs plus its
 //     (max, sum); a small merge kernel combines them.  Single-split sequences write bf16
 //     output directly.
+//   * nv_store_decode_attn (the store of the same forward fused in; kFused): the CTA whose
+//     split holds position L-1 copies the new K/V row from the inputs into its last staged
+//     chunk instead of from the pool, and its consumer warps write that row to its slot.
 #include <mutex>
 
 #include "nv_common.cuh"
@@ -56,6 +59,15 @@ struct DecodeParams {
     int32_t split_tokens;
     int32_t max_splits;
     float scale_log2;   // scale * log2(e)
+    // fused store (nv_store_decode_attn); k_new == nullptr for a plain decode
+    const __nv_bfloat16 *k_new;     // [num_seqs, Hkv, 128], rows k_new_stride elements apart
+    const __nv_bfloat16 *v_new;
+    int64_t k_new_stride;
+    int64_t v_new_stride;
+    const int32_t *slot_mapping;    // [num_seqs]
+    __nv_bfloat16 *k_cache_w;       // the pools, writable (same memory as k_cache / v_cache)
+    __nv_bfloat16 *v_cache_w;
+    int64_t num_slots;
 };
 
 // Reduce G per-lane partial sums over the 16 lanes of a half-warp so that each lane ends
@@ -100,7 +112,7 @@ __device__ __forceinline__ void unpack8(const uint4 &r, float (&f)[8])
     f[7] = bf16hi(r.w);
 }
 
-template <int G, int MAX_KV_HEADS>
+template <int G, int MAX_KV_HEADS, bool kFused>
 __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 2 : 1))
     paged_decode_kernel(const DecodeParams p)
 {
@@ -121,6 +133,8 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
     }
     const int t0 = split * p.split_tokens;
     if (L == 0) {
+        if (kFused && split == 0 && threadIdx.x == 0 && __ldg(p.slot_mapping + b) >= 0)
+            flag_error(p.d_err, NV_DERR_SLOT_MISMATCH);   // a new row for a row with no position L-1
         if (split == 0) {   // padding row: attends to nothing, writes zeros
             uint4 *o = reinterpret_cast<uint4 *>(p.out + (size_t)b * p.num_q_heads * kD);
             for (int i = threadIdx.x; i < p.num_q_heads * kD / 8; i += blockDim.x)
@@ -131,6 +145,28 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
     if (t0 >= L)
         return;
     const int t1 = min(L, t0 + p.split_tokens);
+    // Fused store: the new token is position L-1; its K/V rows come straight from k_new / v_new
+    // (no round trip through the pool) and this CTA also writes them to their slot.  That is only
+    // done when slot_mapping[b] is the slot of position L-1 through the block table; otherwise the
+    // row is not stored, position L-1 is read from the pool, and NV_DERR_SLOT_MISMATCH is set.
+    int new_pos = -1;
+    int64_t new_slot = 0;
+    if (kFused && t1 == L) {                    // only the CTA that holds position L-1
+        const int s = __ldg(p.slot_mapping + b);
+        if (s >= 0) {
+            const int lp = L - 1;
+            const int blk = __ldg(p.block_tables + (size_t)b * p.bt_stride + (lp >> p.block_shift));
+            const int64_t want = ((int64_t)blk << p.block_shift) + (lp & ((1 << p.block_shift) - 1));
+            if (s < p.num_slots && blk >= 0 && blk < p.num_blocks && want == s) {
+                new_pos = lp;
+                new_slot = s;
+            } else if (threadIdx.x == 0) {
+                flag_error(p.d_err, s < p.num_slots ? NV_DERR_SLOT_MISMATCH : NV_DERR_SLOT_RANGE);
+            }
+        } else if (s < -1 && threadIdx.x == 0) {
+            flag_error(p.d_err, NV_DERR_SLOT_RANGE);
+        }
+    }
     const int nsplit = (L + p.split_tokens - 1) / p.split_tokens;
     const int nchunks = (t1 - t0 + kT - 1) / kT;
 
@@ -185,10 +221,21 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
                 if (blk_ok) {
                     valid_rows[s] = n;
                     const int64_t slot = blk_slot0 + (tok0 & bs_mask);
-                    const uint32_t bytes = (uint32_t)n * dkv * 2;
-                    mbar_arrive_expect_tx(full, 2 * bytes);
-                    bulk_g2s(smem_base + s * stage_bytes, p.k_cache + slot * dkv, bytes, full);
-                    bulk_g2s(smem_base + s * stage_bytes + chunk_bytes, p.v_cache + slot * dkv, bytes, full);
+                    const uint32_t row = (uint32_t)dkv * 2;
+                    mbar_arrive_expect_tx(full, 2u * (uint32_t)n * row);
+                    // rows from the pool, except the new token's, which comes from k_new / v_new
+                    const int from_pool = (kFused && new_pos >= tok0 && new_pos < tok0 + n) ? new_pos - tok0 : n;
+                    if (from_pool > 0) {
+                        bulk_g2s(smem_base + s * stage_bytes, p.k_cache + slot * dkv, (uint32_t)from_pool * row, full);
+                        bulk_g2s(smem_base + s * stage_bytes + chunk_bytes, p.v_cache + slot * dkv,
+                                 (uint32_t)from_pool * row, full);
+                    }
+                    if (from_pool < n) {
+                        bulk_g2s(smem_base + s * stage_bytes + (uint32_t)from_pool * row,
+                                 p.k_new + (size_t)b * p.k_new_stride, row, full);
+                        bulk_g2s(smem_base + s * stage_bytes + chunk_bytes + (uint32_t)from_pool * row,
+                                 p.v_new + (size_t)b * p.v_new_stride, row, full);
+                    }
                 } else {
                     valid_rows[s] = 0;     // keys of an out-of-pool block are treated as absent
                     mbar_arrive(full);
@@ -298,6 +345,13 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
                     acc[g][i] = fmaf(pg, vf[i], acc[g][i]);
             }
         }
+        // fused store: this warp writes its kv head of the new row (K by lanes 0-15, V by 16-31)
+        if (kFused && new_pos >= t0 + c * kT && new_pos < t0 + c * kT + kT && nvalid > 0) {
+            const int tok0 = t0 + c * kT;
+            const uint32_t src = (half ? vbase : kbase) + (uint32_t)(new_pos - tok0) * row_bytes;
+            __nv_bfloat16 *dst = (half ? p.v_cache_w : p.k_cache_w) + new_slot * dkv + kvh * kD + sl * 8;
+            *reinterpret_cast<uint4 *>(dst) = lds_u4(src);
+        }
         __syncwarp();
         if (lane == 0)
             mbar_arrive(bar_base + 8 * (kStages + s));
@@ -402,18 +456,18 @@ int decode_split_tokens(int num_seqs, int max_context_len)
     return split;
 }
 
-template <int G, int MAXH>
+template <int G, int MAXH, bool kFused>
 int launch_decode(const DecodeParams &p, int num_seqs, size_t smem_bytes, cudaStream_t stream)
 {
     static bool configured = false;   // benign race: every thread sets the same attribute value
     if (!configured) {
-        if (cudaFuncSetAttribute(paged_decode_kernel<G, MAXH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(paged_decode_kernel<G, MAXH, kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem_bytes > 200 * 1024 ? 227 * 1024 : 200 * 1024) != cudaSuccess)
             return NV_ERR_CUDA;
         configured = true;
     }
     dim3 grid(num_seqs, p.max_splits);
-    paged_decode_kernel<G, MAXH><<<grid, (p.num_kv_heads + 1) * 32, smem_bytes, stream>>>(p);
+    paged_decode_kernel<G, MAXH, kFused><<<grid, (p.num_kv_heads + 1) * 32, smem_bytes, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess)
         return NV_ERR_CUDA;
     if (p.max_splits > 1) {
@@ -424,16 +478,26 @@ int launch_decode(const DecodeParams &p, int num_seqs, size_t smem_bytes, cudaSt
     return NV_OK;
 }
 
-template <int MAXH>
+template <int MAXH, bool kFused>
 int dispatch_group(int group, const DecodeParams &p, int num_seqs, size_t smem, cudaStream_t st)
 {
     switch (group) {
-    case 1: return launch_decode<1, MAXH>(p, num_seqs, smem, st);
-    case 2: return launch_decode<2, MAXH>(p, num_seqs, smem, st);
-    case 4: return launch_decode<4, MAXH>(p, num_seqs, smem, st);
-    case 8: return launch_decode<8, MAXH>(p, num_seqs, smem, st);
+    case 1: return launch_decode<1, MAXH, kFused>(p, num_seqs, smem, st);
+    case 2: return launch_decode<2, MAXH, kFused>(p, num_seqs, smem, st);
+    case 4: return launch_decode<4, MAXH, kFused>(p, num_seqs, smem, st);
+    case 8: return launch_decode<8, MAXH, kFused>(p, num_seqs, smem, st);
     default: return NV_ERR_UNSUPPORTED;
     }
+}
+
+int dispatch(int group, const DecodeParams &p, int num_seqs, size_t smem, cudaStream_t st)
+{
+    const bool fused = p.k_new != nullptr;
+    if (p.num_kv_heads <= 8)
+        return fused ? dispatch_group<8, true>(group, p, num_seqs, smem, st)
+                     : dispatch_group<8, false>(group, p, num_seqs, smem, st);
+    return fused ? dispatch_group<16, true>(group, p, num_seqs, smem, st)
+                 : dispatch_group<16, false>(group, p, num_seqs, smem, st);
 }
 
 }  // namespace
@@ -450,12 +514,21 @@ extern "C" size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q
     return (size_t)num_seqs * max_splits * num_q_heads * (kD + 2) * sizeof(float);
 }
 
-extern "C" int nv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
-                                    const int32_t *block_tables, int32_t bt_stride, const int32_t *context_lens,
-                                    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                    int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
-                                    void *out, void *workspace, size_t workspace_bytes, int32_t *d_err,
-                                    nv_stream_t stream)
+namespace {
+
+struct StoreArgs {     // the new rows of a fused store + decode (absent for a plain decode)
+    const void *k;
+    int64_t k_row_stride;
+    const void *v;
+    int64_t v_row_stride;
+    const int32_t *slot_mapping;
+};
+
+int decode_entry(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                 int32_t bt_stride, const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                 int32_t max_context_len, float scale, void *out, void *workspace, size_t workspace_bytes,
+                 int32_t *d_err, nv_stream_t stream, const StoreArgs *st)
 {
     using namespace nvkv_host;
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || bt_stride <= 0 || num_blocks < 0 ||
@@ -500,6 +573,23 @@ extern "C" int nv_paged_decode_attn(const void *q, const void *k_cache, const vo
     p.split_tokens = decode_split_tokens(num_seqs, max_context_len);
     p.max_splits = (max_len + p.split_tokens - 1) / p.split_tokens;
     p.scale_log2 = scale * nvkv::kLog2e;
+    if (st) {
+        const int64_t dkv = (int64_t)num_kv_heads * kD;
+        if (!st->k || !st->v || !st->slot_mapping)
+            return NV_ERR_NULL;
+        if (st->k_row_stride < dkv || st->v_row_stride < dkv)
+            return NV_ERR_SHAPE;
+        if (st->k_row_stride % 8 != 0 || st->v_row_stride % 8 != 0 || !aligned16(st->k) || !aligned16(st->v))
+            return NV_ERR_ALIGN;
+        p.k_new = static_cast<const __nv_bfloat16 *>(st->k);
+        p.v_new = static_cast<const __nv_bfloat16 *>(st->v);
+        p.k_new_stride = st->k_row_stride;
+        p.v_new_stride = st->v_row_stride;
+        p.slot_mapping = st->slot_mapping;
+        p.k_cache_w = static_cast<__nv_bfloat16 *>(const_cast<void *>(k_cache));
+        p.v_cache_w = static_cast<__nv_bfloat16 *>(const_cast<void *>(v_cache));
+        p.num_slots = (int64_t)num_blocks * block_size;
+    }
     if (p.max_splits > 1) {
         const size_t need = nv_paged_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len);
         if (!workspace || workspace_bytes < need || !aligned16(workspace))
@@ -508,9 +598,35 @@ extern "C" int nv_paged_decode_attn(const void *q, const void *k_cache, const vo
         p.part_ml = p.part_o + (size_t)num_seqs * p.max_splits * num_q_heads * kD;
     }
     const size_t smem = (size_t)kStages * 2 * kT * num_kv_heads * kD * 2 + 2 * kStages * 8 + kStages * 4 + 16;
-    if (num_kv_heads <= 8)
-        return dispatch_group<8>(group, p, num_seqs, smem, (cudaStream_t)stream);
-    return dispatch_group<16>(group, p, num_seqs, smem, (cudaStream_t)stream);
+    return dispatch(group, p, num_seqs, smem, (cudaStream_t)stream);
+}
+
+}  // namespace
+
+extern "C" int nv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *block_tables, int32_t bt_stride, const int32_t *context_lens,
+                                    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
+                                    void *out, void *workspace, size_t workspace_bytes, int32_t *d_err,
+                                    nv_stream_t stream)
+{
+    return decode_entry(q, k_cache, v_cache, block_tables, bt_stride, context_lens, num_seqs, num_q_heads,
+                        num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, out, workspace,
+                        workspace_bytes, d_err, stream, nullptr);
+}
+
+extern "C" int nv_store_decode_attn(const void *q, const void *k, int64_t k_row_stride, const void *v,
+                                    int64_t v_row_stride, const int32_t *slot_mapping, void *k_cache, void *v_cache,
+                                    const int32_t *block_tables, int32_t bt_stride, const int32_t *context_lens,
+                                    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t block_size, int32_t num_blocks, int32_t max_context_len, float scale,
+                                    void *out, void *workspace, size_t workspace_bytes, int32_t *d_err,
+                                    nv_stream_t stream)
+{
+    const StoreArgs st{k, k_row_stride, v, v_row_stride, slot_mapping};
+    return decode_entry(q, k_cache, v_cache, block_tables, bt_stride, context_lens, num_seqs, num_q_heads,
+                        num_kv_heads, head_dim, block_size, num_blocks, max_context_len, scale, out, workspace,
+                        workspace_bytes, d_err, stream, &st);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -624,7 +740,5 @@ extern "C" int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, 
         p.part_ml = p.part_o + (size_t)num_seqs * p.max_splits * num_q_heads * kD;
     }
     const size_t smem = (size_t)kStages * 2 * kT * num_kv_heads * kD * 2 + 2 * kStages * 8 + kStages * 4 + 16;
-    if (num_kv_heads <= 8)
-        return dispatch_group<8>(group, p, num_seqs, smem, (cudaStream_t)stream);
-    return dispatch_group<16>(group, p, num_seqs, smem, (cudaStream_t)stream);
+    return dispatch(group, p, num_seqs, smem, (cudaStream_t)stream);
 }

@@ -87,6 +87,24 @@ def test_decode_validation(lib):
     assert lib.nv_paged_decode_workspace_size(4, 32, 128, 64) == 0   # one split: no workspace
 
 
+def _fused(lib, q=FAKE, k=FAKE, ks=1024, v=FAKE, vs=1024, sm=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, bts=16, cl=FAKE, B=4,
+           hq=32, hkv=8, d=128, bs=256, nb=64, maxc=256, out=FAKE):
+    return lib.nv_store_decode_attn(q, k, ks, v, vs, sm, kc, vc, bt, bts, cl, B, hq, hkv, d, bs, nb, maxc, 0.088, out,
+                                    None, 0, None, None)
+
+
+def test_fused_store_decode_validation(lib):
+    assert _fused(lib, B=0, q=None) == 0
+    assert _fused(lib, k=None) == NV_ERR_NULL
+    assert _fused(lib, sm=None) == NV_ERR_NULL
+    assert _fused(lib, q=None) == NV_ERR_NULL
+    assert _fused(lib, ks=512) == NV_ERR_SHAPE              # row stride below Hkv*D
+    assert _fused(lib, vs=1028) == NV_ERR_ALIGN             # not a multiple of 8 elements
+    assert _fused(lib, v=MISALIGNED) == NV_ERR_ALIGN
+    assert _fused(lib, d=64) == NV_ERR_UNSUPPORTED
+    assert _fused(lib, maxc=4096) == NV_ERR_WORKSPACE       # several splits need a workspace
+
+
 def _prefill(lib, q=FAKE, kc=FAKE, vc=FAKE, cq=FAKE, ck=FAKE, bt=FAKE, bts=8, B=2, tq=100, mq=80, hq=16, hkv=8,
              d=128, bs=256, nb=16, out=FAKE, ws=FAKE, wsb=256):
     return lib.nv_paged_prefill_attn(q, kc, vc, cq, ck, bt, bts, B, tq, mq, hq, hkv, d, bs, nb, 0.088, out, ws, wsb,
