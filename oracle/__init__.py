@@ -59,6 +59,8 @@ def _load(path: str):
     L.oracle_decode_attn.restype = i32
     L.oracle_prefill_attn.argtypes = [P, P, P, P, P, P, i32, i32, P, i64, i32, i32, i32, i32, f32, P]
     L.oracle_prefill_attn.restype = i32
+    L.oracle_qk_norm_rope_store.argtypes = [P, i64, P, P, P, f32, f32, P, i64, i32, i32, i32, P, P, P, i64]
+    L.oracle_qk_norm_rope_store.restype = i64
     return L
 
 
@@ -171,6 +173,27 @@ class Oracle:
         _parallel(run, rows.shape[0], threads)
         return out
 
+    def qk_norm_rope_store(self, qkv, positions, q_weight, k_weight, eps, theta, slot_mapping, num_q_heads,
+                           num_kv_heads, k_cache, v_cache):
+        """QK-norm + RoPE + store: returns ``(q_out [N, Hq, D] uint16, rejected)``; stores into the caches.
+
+        ``qkv``: uint16 ``[N, row_stride]`` (q | k | v per row); caches as for ``store_kvcache``."""
+        qkv = np.asarray(qkv)
+        assert qkv.dtype == np.uint16 and qkv.ndim == 2 and qkv.strides[1] == 2
+        n = qkv.shape[0]
+        d = int(np.asarray(q_weight).shape[0])
+        pos = _c(positions, np.int32)
+        sm = _c(slot_mapping, np.int32)
+        qw, kw = _c(q_weight, np.uint16), _c(k_weight, np.uint16)
+        assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+        num_slots = k_cache.size // (num_kv_heads * d)
+        q_out = np.zeros((n, num_q_heads, d), np.uint16)
+        stride = qkv.strides[0] // 2 if n else qkv.shape[1]
+        rej = self.lib.oracle_qk_norm_rope_store(_ptr(qkv), stride, _ptr(pos), _ptr(qw), _ptr(kw), float(eps),
+                                                 float(theta), _ptr(sm), n, int(num_q_heads), int(num_kv_heads), d,
+                                                 _ptr(q_out), _ptr(k_cache), _ptr(v_cache), num_slots)
+        return q_out, int(rej)
+
 
 def slot_of(table, pos, block_size):
     return default().slot_of(table, pos, block_size)
@@ -186,6 +209,10 @@ def decode_attn(*args, **kw):
 
 def prefill_attn(*args, **kw):
     return default().prefill_attn(*args, **kw)
+
+
+def qk_norm_rope_store(*args, **kw):
+    return default().qk_norm_rope_store(*args, **kw)
 
 
 def _parallel(run, n, threads):

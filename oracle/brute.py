@@ -78,3 +78,28 @@ def prefill(q, k_cache4, v_cache4, cu_q, cu_k, block_tables, scale):
         V = widen(unpage(v_cache4, block_tables[b], Lk))
         out[q0:q1] = attention(q[q0:q1], K, V, scale, Lk - (q1 - q0))
     return out
+
+
+def round_bf16(x) -> np.ndarray:
+    """Round to bf16 (nearest even) and widen back to float64; via float32, then the bit trick."""
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint32) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def norm_rope(x_bits, w_bits, eps, theta, positions):
+    """Float64 restatement of Qwen3's QK-norm + RoPE for head vectors ``x_bits`` ``[N, H, D]``
+    (bf16 bits) at ``positions`` ``[N]``: RMSNorm over D (cast to bf16, then the bf16 product with
+    the weight), then the rotate-half rotation by position * theta^(-2j/D).  Returns float64
+    values already rounded to bf16 (the pages' output dtype)."""
+    x = widen(x_bits)
+    w = widen(w_bits)
+    d = x.shape[-1]
+    r = 1.0 / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps)
+    n = round_bf16(round_bf16(x * r) * w)
+    j = np.arange(d // 2, dtype=np.float64)
+    ang = np.asarray(positions, np.float64)[:, None, None] * theta ** (-2.0 * j / d)
+    x1, x2 = n[..., : d // 2], n[..., d // 2:]
+    return np.concatenate([round_bf16(x1 * np.cos(ang) - x2 * np.sin(ang)),
+                           round_bf16(x2 * np.cos(ang) + x1 * np.sin(ang))], axis=-1)

@@ -190,3 +190,92 @@ int32_t oracle_prefill_attn(const uint16_t *q, const uint16_t *k_cache, const ui
     free(work);
     return 0;
 }
+
+/* ------------------------------------------------------------------------------------
+ * QK-norm + RoPE + store (the attention layer's prologue).
+ *
+ * Field guide, "Qwen3Attention.forward": the fused projection output of each token is split into
+ * q [Hq, D], k [Hkv, D], v [Hkv, D]; q and k go through Qwen3's QK-norm (an RMSNorm over each
+ * head's D values, before RoPE), then RoPE at the token's position; k and v are then stored at
+ * the token's slot (Step 10.3) and q goes on to attention.
+ *   RMSNorm ("layernorm.py"): statistics in float32 -- var = mean(x^2), x * rsqrt(var + eps) --
+ *   the result cast back to bf16, THEN multiplied by the bf16 weight (a bf16 product).
+ *   RoPE ("rotary_embedding.py"): frequencies inv_freq_j = 1 / base^(2j / D) (float32),
+ *   angle = position * inv_freq_j (float32), rotate-half layout: element j pairs with element
+ *   j + D/2; y1 = x1 cos - x2 sin, y2 = x2 cos + x1 sin in float32, cast to bf16.
+ * ------------------------------------------------------------------------------------ */
+
+/* float -> bf16 bit pattern, round to nearest even (NaN kept quiet). */
+static uint16_t round_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return (uint16_t)((u >> 16) | 0x40u);
+    const uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/* One head vector x (D bf16 values): RMSNorm with weight w, then RoPE at `pos`; bf16 out. */
+static void norm_rope_head(const uint16_t *x, const uint16_t *w, int32_t d, float eps, float theta, int32_t pos,
+                           uint16_t *y)
+{
+    float ss = 0.0f;
+    for (int32_t i = 0; i < d; ++i) {
+        const float xi = widen_bf16(x[i]);
+        ss += xi * xi;
+    }
+    const float var = ss / (float)d;
+    const float r = 1.0f / sqrtf(var + eps);
+    float n[256];
+    for (int32_t i = 0; i < d; ++i) {
+        const uint16_t cast = round_bf16(widen_bf16(x[i]) * r);            /* x.to(orig_dtype) */
+        n[i] = widen_bf16(round_bf16(widen_bf16(cast) * widen_bf16(w[i])));   /* .mul_(weight) in bf16 */
+    }
+    const int32_t half = d / 2;
+    for (int32_t j = 0; j < half; ++j) {
+        const float inv_freq = 1.0f / powf(theta, (float)(2 * j) / (float)d);
+        const float angle = (float)pos * inv_freq;
+        const float c = cosf(angle), s = sinf(angle);
+        const float x1 = n[j], x2 = n[j + half];
+        y[j] = round_bf16(x1 * c - x2 * s);
+        y[j + half] = round_bf16(x2 * c + x1 * s);
+    }
+}
+
+/* For each token t < n: row t of qkv holds [Hq*D q | Hkv*D k | Hkv*D v] (row_stride elements
+ * apart).  q heads -> normed + roped -> q_out[t] ([Hq, D]); k heads -> normed + roped -> row
+ * slot_mapping[t] of k_cache; v -> copied unchanged to row slot_mapping[t] of v_cache.  A slot of
+ * -1 stores nothing (q is still produced); other slots outside [0, num_slots) are skipped and
+ * counted (the return value). */
+int64_t oracle_qk_norm_rope_store(const uint16_t *qkv, int64_t row_stride, const int32_t *positions,
+                                  const uint16_t *q_weight, const uint16_t *k_weight, float eps, float theta,
+                                  const int32_t *slot_mapping, int64_t n, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, uint16_t *q_out, uint16_t *k_cache, uint16_t *v_cache,
+                                  int64_t num_slots)
+{
+    int64_t rejected = 0;
+    const int64_t dkv = (int64_t)num_kv_heads * head_dim;
+    for (int64_t t = 0; t < n; ++t) {
+        const uint16_t *row = qkv + t * row_stride;
+        const int32_t pos = positions[t];
+        for (int32_t h = 0; h < num_q_heads; ++h)
+            norm_rope_head(row + (int64_t)h * head_dim, q_weight, head_dim, eps, theta, pos,
+                           q_out + (t * num_q_heads + h) * head_dim);
+        const int32_t slot = slot_mapping[t];
+        if (slot == -1)
+            continue;
+        if (slot < -1 || slot >= num_slots) {
+            ++rejected;
+            continue;
+        }
+        const uint16_t *krow = row + (int64_t)num_q_heads * head_dim;
+        const uint16_t *vrow = krow + dkv;
+        for (int32_t h = 0; h < num_kv_heads; ++h)
+            norm_rope_head(krow + (int64_t)h * head_dim, k_weight, head_dim, eps, theta, pos,
+                           k_cache + slot * dkv + (int64_t)h * head_dim);
+        memcpy(v_cache + slot * dkv, vrow, (size_t)dkv * sizeof(uint16_t));
+    }
+    return rejected;
+}

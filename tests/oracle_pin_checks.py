@@ -298,7 +298,128 @@ def check_causal_alignment_spike(orc):
     np.testing.assert_allclose(out[:, 0, :], V[P:Lk], rtol=0, atol=1e-3)
 
 
+# ---------------------------------------------------------------------------
+# attention prologue: QK-norm + RoPE + store
+# ---------------------------------------------------------------------------
+
+def _bf16_ulp(v):
+    """One bf16 ulp at each |v| (>= the smallest normal's)."""
+    e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def _prologue_case(n=6, hq=4, hkv=2, d=128, seed=3, positions=None):
+    rng = np.random.default_rng([seed, 77])
+    qkv = W.normal_bf16(rng, (n, (hq + 2 * hkv) * d))
+    w = W.f32_to_bf16_bits(1.0 + 0.1 * rng.standard_normal((2, d)).astype(np.float32))
+    pos = np.asarray(positions if positions is not None else rng.integers(0, 5000, n), np.int32)
+    return qkv, w[0].copy(), w[1].copy(), pos
+
+
+def _run_prologue(orc, qkv, qw, kw, pos, hq, hkv, slots=None, num_slots=None, eps=1e-6, theta=1e6):
+    n = qkv.shape[0]
+    d = qw.shape[0]
+    slots = np.arange(n, dtype=np.int32) if slots is None else np.asarray(slots, np.int32)
+    num_slots = n if num_slots is None else num_slots
+    kc = np.full((num_slots, hkv * d), 0x7FC1, np.uint16)
+    vc = np.full((num_slots, hkv * d), 0x7FC1, np.uint16)
+    q, rej = orc.qk_norm_rope_store(qkv, pos, qw, kw, eps, theta, slots, hq, hkv, kc, vc)
+    return q, kc, vc, rej
+
+
+def check_prologue_brute_force(orc):
+    """The C oracle against a float64 restatement: within one bf16 ulp, and equal nearly everywhere."""
+    hq, hkv, d = 4, 2, 128
+    qkv, qw, kw, pos = _prologue_case(hq=hq, hkv=hkv)
+    q, kc, vc, _ = _run_prologue(orc, qkv, qw, kw, pos, hq, hkv)
+    n = qkv.shape[0]
+    xq = qkv[:, :hq * d].reshape(n, hq, d)
+    xk = qkv[:, hq * d:(hq + hkv) * d].reshape(n, hkv, d)
+    for got_bits, x, w in ((q, xq, qw), (kc.reshape(n, hkv, d), xk, kw)):
+        got = brute.widen(got_bits)
+        want = brute.norm_rope(x, w, 1e-6, 1e6, pos)
+        diff = np.abs(got - want)
+        # the pages form each angle in fp32 (position * frequency): up to pos * 2^-24 rad away from
+        # the float64 angle, which moves an output by at most that times the pair's magnitude
+        mag = np.abs(want).max(axis=-1, keepdims=True) * 2.0
+        tol = _bf16_ulp(want) * 1.01 + mag * pos[:, None, None] * 2.0 ** -23
+        assert (diff <= tol).all(), (diff - tol).max()
+        assert (diff > 0).mean() < 0.05, (diff > 0).mean()
+    # v is stored unchanged
+    assert np.array_equal(vc, qkv[:, (hq + hkv) * d:])
+
+
+def check_prologue_position_zero_is_norm_only(orc):
+    """At position 0 every angle is 0: the output is the normalised, weighted input, whatever theta."""
+    hq, hkv, d = 2, 1, 128
+    qkv, qw, kw, _ = _prologue_case(n=3, hq=hq, hkv=hkv, positions=[0, 0, 0])
+    pos = np.zeros(3, np.int32)
+    a = _run_prologue(orc, qkv, qw, kw, pos, hq, hkv, theta=1e6)
+    b = _run_prologue(orc, qkv, qw, kw, pos, hq, hkv, theta=10.0)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    x = brute.widen(qkv[:, :hq * d].reshape(3, hq, d))
+    r = 1.0 / np.sqrt((x * x).mean(axis=-1, keepdims=True) + 1e-6)
+    want = brute.round_bf16(brute.round_bf16(x * r) * brute.widen(qw))
+    assert (np.abs(brute.widen(a[0]) - want) <= _bf16_ulp(want) * 1.01).all()
+
+
+def check_prologue_rope_closed_form(orc):
+    """A head vector with one nonzero value a at dim j normalises to sqrt(D) * sign(a) (weight 1),
+    and RoPE turns it into (v cos phi, v sin phi) at dims (j, j + D/2), phi = pos * theta^(-2j/D)."""
+    hq, hkv, d = 1, 1, 128
+    theta = 1e6
+    one = np.full(d, 0x3F80, np.uint16)                       # weight 1.0
+    for j, pos in ((0, 1), (0, 1000), (1, 4095), (5, 77), (63, 3000)):
+        qkv = np.zeros((1, 3 * d), np.uint16)
+        qkv[0, j] = 0x3FC0                                     # 1.5
+        q, _, _, _ = _run_prologue(orc, qkv, one, one, np.array([pos], np.int32), hq, hkv, theta=theta)
+        v = float(brute.round_bf16(np.sqrt(d / (1.0 + 1e-6 * d / 2.25))))   # bf16 of the normalised value
+        phi = pos * theta ** (-2.0 * j / d)
+        got = brute.widen(q[0, 0])
+        want = np.zeros(d)
+        want[j], want[j + d // 2] = v * np.cos(phi), v * np.sin(phi)
+        want = brute.round_bf16(want)
+        assert (np.abs(got - want) <= _bf16_ulp(want) * 1.01 + 1e-6).all(), (j, pos, got[j], want[j])
+
+
+def check_prologue_relative_position(orc):
+    """RoPE makes <q(p), k(p')> depend only on p - p': shifting both positions leaves it unchanged."""
+    hq, hkv, d = 1, 1, 128
+    one = np.full(d, 0x3F80, np.uint16)
+    rng = np.random.default_rng(5)
+    qkv = W.normal_bf16(rng, (1, 3 * d))
+    qkv2 = np.repeat(qkv, 4, axis=0)
+    pos = np.array([700, 400, 1700, 1400], np.int32)           # pairs (700, 400) and (1700, 1400)
+    q, kc, _, _ = _run_prologue(orc, qkv2, one, one, pos, hq, hkv)
+    qf, kf = brute.widen(q[:, 0]), brute.widen(kc)
+    d1 = float(qf[0] @ kf[1])
+    d2 = float(qf[2] @ kf[3])
+    assert abs(d1 - d2) <= 0.02 * (abs(d1) + 1.0), (d1, d2)
+    d3 = float(qf[0] @ kf[3])                                  # a different offset changes it
+    assert abs(d3 - d1) > 0.05 * (abs(d1) + 1.0)
+
+
+def check_prologue_zero_vector_and_slots(orc):
+    """A zero head vector stays zero (eps keeps it finite); slot -1 stores nothing but q is
+    produced; slots outside the pool are counted and skipped."""
+    hq, hkv, d = 2, 1, 128
+    qkv, qw, kw, pos = _prologue_case(n=4, hq=hq, hkv=hkv)
+    qkv[0, :] = 0
+    q, kc, vc, rej = _run_prologue(orc, qkv, qw, kw, pos, hq, hkv, slots=[0, -1, 7, 1], num_slots=3)
+    assert not brute.widen(q[0]).any() and np.isfinite(brute.widen(q)).all()
+    assert not brute.widen(kc[0]).any()
+    assert rej == 1
+    assert (kc[2] == 0x7FC1).all() and (vc[2] == 0x7FC1).all()      # nothing for tokens 1 (-1) and 2 (7)
+    assert brute.widen(q[1]).any()
+    assert np.array_equal(vc[1], qkv[3, (hq + hkv) * d:])
+
+
 ALL_CHECKS = [
+    check_prologue_brute_force,
+    check_prologue_position_zero_is_norm_only,
+    check_prologue_rope_closed_form,
+    check_prologue_relative_position,
+    check_prologue_zero_vector_and_slots,
     check_slot_examples,
     check_store_tiny,
     check_store_padding_and_range,

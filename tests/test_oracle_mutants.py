@@ -28,6 +28,17 @@ MUTANTS = {
                             "h % num_kv_heads, head_dim, scale, work, out + r);"),
     "value_from_key_cache": ("const uint16_t *vr = v_cache +", "const uint16_t *vr = k_cache +"),
     "zero_len_not_zero": ("out[t] = 0.0f;\n        return;", "out[t] = 1.0f;\n        return;"),
+    # attention prologue (QK-norm + RoPE + store)
+    "rope_adjacent_pairs": ("const float x1 = n[j], x2 = n[j + half];", "const float x1 = n[2 * j], x2 = n[2 * j + 1];"),
+    "rope_sign_flip": ("y[j] = round_bf16(x1 * c - x2 * s);", "y[j] = round_bf16(x1 * c + x2 * s);"),
+    "rope_freq_not_inverted": ("const float inv_freq = 1.0f / powf(", "const float inv_freq = 1.0f * powf("),
+    "rope_freq_index_j": ("(float)(2 * j) / (float)d", "(float)(j) / (float)d"),
+    "norm_eps_dropped": ("sqrtf(var + eps)", "sqrtf(var)"),
+    "norm_mean_not_divided": ("const float var = ss / (float)d;", "const float var = ss;"),
+    "norm_weight_dropped": ("round_bf16(widen_bf16(cast) * widen_bf16(w[i]))", "round_bf16(widen_bf16(cast))"),
+    "k_normed_with_q_weight": ("norm_rope_head(krow + (int64_t)h * head_dim, k_weight,",
+                               "norm_rope_head(krow + (int64_t)h * head_dim, q_weight,"),
+    "v_stored_from_k": ("memcpy(v_cache + slot * dkv, vrow,", "memcpy(v_cache + slot * dkv, krow,"),
 }
 
 _RUNNER = r"""

@@ -31,6 +31,7 @@ BF16_NAN_SENTINEL = np.uint16(0x7FC1)   # quiet-NaN pattern used to poison slots
 _TAG_CACHE_K = 1
 _TAG_CACHE_V = 2
 _TAG_QKV = 3
+_TAG_PROLOGUE = 4
 
 
 # ----------------------------------------------------------------------------
@@ -259,6 +260,35 @@ def _new_rows(seed, n, hq, hkv, d):
     k = normal_bf16(rng, (n, hkv, d))
     v = normal_bf16(rng, (n, hkv, d))
     return q, k, v
+
+
+@dataclass
+class PrologueInputs:
+    """Inputs of the attention prologue (QK-norm + RoPE + store) for the new rows of a batch."""
+    qkv: np.ndarray          # uint16 [N, (Hq + 2 Hkv) * D]: q | k | v of each new token
+    positions: np.ndarray    # int32 [N]
+    q_weight: np.ndarray     # uint16 [D]
+    k_weight: np.ndarray     # uint16 [D]
+    eps: float
+    theta: float
+
+
+def prologue_inputs(batch: "PagedBatch", seed: int = 0, eps: float = 1e-6, theta: float = 1e6) -> PrologueInputs:
+    """Projection rows N(0,1) (bf16) for every new token of ``batch`` (one per slot_mapping entry),
+    the tokens' positions (prefix + index for prefill, L-1 for decode, 0 for padding rows), and
+    random-init norm weights N(1, 0.1^2) (bf16) -- Qwen3's layer shapes with synthetic values."""
+    rng = np.random.default_rng([seed, _TAG_PROLOGUE])
+    n = int(batch.slot_mapping.shape[0])
+    width = (batch.num_q_heads + 2 * batch.num_kv_heads) * batch.head_dim
+    qkv = normal_bf16(rng, (n, width))
+    w = f32_to_bf16_bits(1.0 + 0.1 * rng.standard_normal((2, batch.head_dim)).astype(np.float32))
+    if batch.kind == "decode":
+        pos = np.maximum(batch.seq_lens.astype(np.int64) - 1, 0)
+    else:
+        pos = np.concatenate([np.arange(int(p), int(p) + int(lq)) for p, lq in
+                              zip(batch.meta["prefix_lens"], batch.q_lens)]) if n else np.zeros(0, np.int64)
+    return PrologueInputs(qkv=qkv, positions=pos.astype(np.int32), q_weight=w[0].copy(), k_weight=w[1].copy(),
+                          eps=float(eps), theta=float(theta))
 
 
 def make_decode(name, seed, ctx_lens, hq, hkv, d, block_size, n_pad=0, width=None,
