@@ -90,6 +90,35 @@ int nv_store_kvcache(const void *k, int64_t k_row_stride, const void *v, int64_t
                      nv_stream_t stream);
 
 /*
+ * nv_qk_norm_rope_store -- the attention layer's prologue: QK-norm, RoPE, then the K/V store.
+ *
+ * Field guide, "Qwen3Attention.forward" with "layernorm.py" and "rotary_embedding.py", and Step
+ * 10.3: each token's fused projection row is split into q [Hq, D], k [Hkv, D], v [Hkv, D].  Every
+ * q and k head is RMS-normalised over its D values -- var = mean(x^2) in fp32, x * rsqrt(var +
+ * eps) cast to bf16, then multiplied by the bf16 weight (q_norm_weight / k_norm_weight, [D]) as a
+ * bf16 product -- and then rotated by RoPE at positions[t]: element j pairs with j + D/2
+ * (rotate-half), angle = positions[t] * rope_theta^(-2j/D) in fp32, y1 = x1 cos - x2 sin,
+ * y2 = x2 cos + x1 sin in fp32, rounded to bf16.  q goes to q_out; the roped k and the unchanged
+ * v are written to row slot_mapping[t] of the caches (-1 = store nothing; q is still produced).
+ *
+ *   qkv           bf16 [n_tokens, row stride qkv_row_stride elements] holding q | k | v
+ *                 (>= (Hq + 2 Hkv) * head_dim, multiple of 8); 16-byte aligned.
+ *   positions     int32 [n_tokens] (< 2^24).
+ *   q_norm_weight, k_norm_weight  bf16 [head_dim], 4-byte aligned.
+ *   q_out         bf16 [n_tokens, Hq, head_dim] contiguous.
+ *   k_cache, v_cache  as for nv_store_kvcache ([num_slots, Hkv*head_dim] flattened).
+ *   rms_eps >= 0 (1e-6 in Qwen3); rope_theta > 1 (1e6 in Qwen3).
+ *   d_err         nullable; NV_DERR_SLOT_RANGE for slots outside [-1, num_slots) (row not stored).
+ * head_dim must be 128.  Results are within a bf16 rounding of the fp32 definition (the GPU's
+ * rsqrt / sincos differ from a CPU libm by an ulp or two of fp32); v is copied bit for bit.
+ */
+int nv_qk_norm_rope_store(const void *qkv, int64_t qkv_row_stride, const int32_t *positions,
+                          const void *q_norm_weight, const void *k_norm_weight, float rms_eps, float rope_theta,
+                          const int32_t *slot_mapping, int32_t n_tokens, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, void *q_out, void *k_cache, void *v_cache, int64_t num_slots,
+                          int32_t *d_err, nv_stream_t stream);
+
+/*
  * Bytes of workspace nv_paged_decode_attn needs for this batch (0 means none).  Depends only
  * on its arguments, so it can be sized once for the largest batch and reused.
  */

@@ -88,16 +88,21 @@ def round_bf16(x) -> np.ndarray:
     return r.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
+def rms_norm(x_bits, w_bits, eps):
+    """Qwen3's per-head RMSNorm in float64: x / sqrt(mean(x^2) + eps) rounded to bf16, then the
+    bf16 product with the weight (rounded to bf16)."""
+    x = widen(x_bits)
+    r = 1.0 / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps)
+    return round_bf16(round_bf16(x * r) * widen(w_bits))
+
+
 def norm_rope(x_bits, w_bits, eps, theta, positions):
     """Float64 restatement of Qwen3's QK-norm + RoPE for head vectors ``x_bits`` ``[N, H, D]``
     (bf16 bits) at ``positions`` ``[N]``: RMSNorm over D (cast to bf16, then the bf16 product with
     the weight), then the rotate-half rotation by position * theta^(-2j/D).  Returns float64
     values already rounded to bf16 (the pages' output dtype)."""
-    x = widen(x_bits)
-    w = widen(w_bits)
-    d = x.shape[-1]
-    r = 1.0 / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps)
-    n = round_bf16(round_bf16(x * r) * w)
+    n = rms_norm(x_bits, w_bits, eps)
+    d = n.shape[-1]
     j = np.arange(d // 2, dtype=np.float64)
     ang = np.asarray(positions, np.float64)[:, None, None] * theta ** (-2.0 * j / d)
     x1, x2 = n[..., : d // 2], n[..., d // 2:]

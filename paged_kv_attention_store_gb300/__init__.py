@@ -31,7 +31,7 @@ NV_DERR_SLOT_MISMATCH = 0x10
 
 EXPORTED = ("nv_status_string", "nv_store_kvcache", "nv_paged_decode_workspace_size", "nv_paged_decode_attn",
             "nv_store_decode_attn", "nv_paged_decode_attn_noalloc", "nv_paged_prefill_workspace_size",
-            "nv_paged_prefill_attn")
+            "nv_paged_prefill_attn", "nv_qk_norm_rope_store")
 
 
 class NvError(RuntimeError):
@@ -65,6 +65,8 @@ def load_library(path: str | None = None):
     L.nv_paged_decode_workspace_size.restype = sz
     L.nv_paged_decode_attn.argtypes = [V, V, V, V, i32, V, i32, i32, i32, i32, i32, i32, i32, f32, V, V, sz, V, V]
     L.nv_paged_decode_attn.restype = ctypes.c_int
+    L.nv_qk_norm_rope_store.argtypes = [V, i64, V, V, V, f32, f32, V, i32, i32, i32, i32, V, V, V, i64, V, V]
+    L.nv_qk_norm_rope_store.restype = ctypes.c_int
     L.nv_store_decode_attn.argtypes = [V, V, i64, V, i64, V, V, V, V, i32, V, i32, i32, i32, i32, i32, i32, i32, f32,
                                        V, V, sz, V, V]
     L.nv_store_decode_attn.restype = ctypes.c_int
@@ -120,6 +122,27 @@ def nv_store_kvcache(k, v, slot_mapping, k_cache, v_cache, d_err=None, stream=No
     rc = load_library().nv_store_kvcache(_ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(slot_mapping), n,
                                          _ptr(k_cache), _ptr(v_cache), nb * bs, hkv, d, _ptr(d_err), _stream(stream))
     _check("nv_store_kvcache", rc)
+
+
+def nv_qk_norm_rope_store(qkv, positions, q_norm_weight, k_norm_weight, slot_mapping, k_cache, v_cache,
+                          num_q_heads, rms_eps=1e-6, rope_theta=1e6, q_out=None, d_err=None, stream=None):
+    """QK-norm + RoPE on the q and k heads of ``qkv`` ``[N, (Hq + 2 Hkv) * D]`` (rows may be strided),
+    roped q returned (``[N, Hq, D]``), roped k and v stored at ``slot_mapping`` (-1 = skip)."""
+    import torch
+    nb, bs, hkv, d = _pool_shape(k_cache, v_cache)
+    _need(qkv.dim() == 2 and qkv.stride(1) == 1, "qkv must be [N, row] with unit column stride")
+    n = int(qkv.shape[0])
+    _need(int(qkv.shape[1]) >= (num_q_heads + 2 * hkv) * d, "qkv rows are too short for q | k | v")
+    _need(int(positions.shape[0]) == n and int(slot_mapping.shape[0]) == n, "one position and slot per token")
+    _need(q_norm_weight.numel() == d and k_norm_weight.numel() == d, "norm weights must have head_dim values")
+    if q_out is None:
+        q_out = torch.empty((n, num_q_heads, d), dtype=qkv.dtype, device=qkv.device)
+    rc = load_library().nv_qk_norm_rope_store(
+        _ptr(qkv), qkv.stride(0), _ptr(positions), _ptr(q_norm_weight), _ptr(k_norm_weight), float(rms_eps),
+        float(rope_theta), _ptr(slot_mapping), n, int(num_q_heads), hkv, d, _ptr(q_out), _ptr(k_cache),
+        _ptr(v_cache), nb * bs, _ptr(d_err), _stream(stream))
+    _check("nv_qk_norm_rope_store", rc)
+    return q_out
 
 
 def nv_paged_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len) -> int:

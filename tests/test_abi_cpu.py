@@ -105,6 +105,23 @@ def test_fused_store_decode_validation(lib):
     assert _fused(lib, maxc=4096) == NV_ERR_WORKSPACE       # several splits need a workspace
 
 
+def _prologue(lib, qkv=FAKE, rs=4096, pos=FAKE, qw=FAKE, kw=FAKE, sm=FAKE, n=4, hq=16, hkv=8, d=128, qo=FAKE,
+              kc=FAKE, vc=FAKE, slots=64, eps=1e-6, theta=1e6):
+    return lib.nv_qk_norm_rope_store(qkv, rs, pos, qw, kw, eps, theta, sm, n, hq, hkv, d, qo, kc, vc, slots, None, None)
+
+
+def test_prologue_validation(lib):
+    assert _prologue(lib, n=0, qkv=None) == 0
+    assert _prologue(lib, qkv=None) == NV_ERR_NULL
+    assert _prologue(lib, kw=None) == NV_ERR_NULL
+    assert _prologue(lib, d=64, rs=2048) == NV_ERR_UNSUPPORTED
+    assert _prologue(lib, rs=4088) == NV_ERR_SHAPE           # row shorter than q | k | v
+    assert _prologue(lib, rs=4100) == NV_ERR_ALIGN           # not a multiple of 8 elements
+    assert _prologue(lib, qo=MISALIGNED) == NV_ERR_ALIGN
+    assert _prologue(lib, theta=1.0) == NV_ERR_SHAPE
+    assert _prologue(lib, eps=-1.0) == NV_ERR_SHAPE
+
+
 def _prefill(lib, q=FAKE, kc=FAKE, vc=FAKE, cq=FAKE, ck=FAKE, bt=FAKE, bts=8, B=2, tq=100, mq=80, hq=16, hkv=8,
              d=128, bs=256, nb=16, out=FAKE, ws=FAKE, wsb=256):
     return lib.nv_paged_prefill_attn(q, kc, vc, cq, ck, bt, bts, B, tq, mq, hq, hkv, d, bs, nb, 0.088, out, ws, wsb,
