@@ -61,6 +61,10 @@ def _load(path: str):
     L.oracle_prefill_attn.restype = i32
     L.oracle_qk_norm_rope_store.argtypes = [P, i64, P, P, P, f32, f32, P, i64, i32, i32, i32, P, P, P, i64]
     L.oracle_qk_norm_rope_store.restype = i64
+    L.oracle_prepare_decode.argtypes = [P, P, i32, i32, i32, i32, P, P, P]
+    L.oracle_prepare_decode.restype = i64
+    L.oracle_prepare_prefill.argtypes = [P, P, P, i32, i32, i32, P, P, P, P, P]
+    L.oracle_prepare_prefill.restype = i64
     return L
 
 
@@ -193,6 +197,31 @@ class Oracle:
                                                  float(theta), _ptr(sm), n, int(num_q_heads), int(num_kv_heads), d,
                                                  _ptr(q_out), _ptr(k_cache), _ptr(v_cache), num_slots)
         return q_out, int(rej)
+
+    def prepare_decode(self, seq_lens, block_tables, block_size, padded_seqs=None):
+        """``(context_lens, positions, slot_mapping, bad_rows)`` for a decode step (int32 arrays)."""
+        sl = _c(seq_lens, np.int32)
+        bt = _c(block_tables, np.int32)
+        b = sl.shape[0]
+        pad = b if padded_seqs is None else int(padded_seqs)
+        cl, pos, sm = (np.zeros(pad, np.int32) for _ in range(3))
+        bad = self.lib.oracle_prepare_decode(_ptr(sl), _ptr(bt), bt.shape[1], b, pad, int(block_size), _ptr(cl),
+                                             _ptr(pos), _ptr(sm))
+        return cl, pos, sm, int(bad)
+
+    def prepare_prefill(self, num_cached, num_scheduled, block_tables, block_size):
+        """``(cu_seqlens_q, cu_seqlens_k, positions, slot_mapping, (max_seqlen_q, max_seqlen_k))``."""
+        nc, ns = _c(num_cached, np.int32), _c(num_scheduled, np.int32)
+        bt = _c(block_tables, np.int32)
+        b = nc.shape[0]
+        total = int(ns.sum())
+        cq, ck = np.zeros(b + 1, np.int32), np.zeros(b + 1, np.int32)
+        pos, sm = np.zeros(max(total, 1), np.int32), np.zeros(max(total, 1), np.int32)
+        mx = np.zeros(2, np.int32)
+        n = self.lib.oracle_prepare_prefill(_ptr(nc), _ptr(ns), _ptr(bt), bt.shape[1], b, int(block_size), _ptr(cq),
+                                            _ptr(ck), _ptr(pos), _ptr(sm), _ptr(mx))
+        assert n == total, n
+        return cq, ck, pos[:total], sm[:total], (int(mx[0]), int(mx[1]))
 
 
 def slot_of(table, pos, block_size):

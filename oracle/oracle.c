@@ -279,3 +279,85 @@ int64_t oracle_qk_norm_rope_store(const uint16_t *qkv, int64_t row_stride, const
     }
     return rejected;
 }
+
+/* ------------------------------------------------------------------------------------
+ * Attention metadata (the model runner's prepare_decode / prepare_prefill).
+ * ------------------------------------------------------------------------------------ */
+
+/* Field guide Step 07.6 "prepare_decode: one token per sequence": for sequence b with len(seq) =
+ * seq_lens[b] tokens (the new one included), position = len - 1, context_len = len, and the slot is
+ * the last block's base slot plus last_block_num_tokens - 1, i.e. the slot of position len - 1.
+ * Step 07.8 graph replay: rows num_seqs .. padded_seqs-1 get slot -1 and context 0 (position 0).
+ * A row whose length is < 1 or needs a block the table does not hold gets slot -1 / context 0;
+ * the count of such rows is returned. */
+int64_t oracle_prepare_decode(const int32_t *seq_lens, const int32_t *block_tables, int32_t bt_stride,
+                              int32_t num_seqs, int32_t padded_seqs, int32_t block_size, int32_t *context_lens,
+                              int32_t *positions, int32_t *slot_mapping)
+{
+    int64_t bad = 0;
+    for (int32_t b = 0; b < padded_seqs; ++b) {
+        context_lens[b] = 0;
+        positions[b] = 0;
+        slot_mapping[b] = -1;
+        if (b >= num_seqs)
+            continue;
+        const int32_t len = seq_lens[b];
+        const int32_t nblocks = (len + block_size - 1) / block_size;
+        if (len < 1 || nblocks > bt_stride) {
+            ++bad;
+            continue;
+        }
+        const int32_t last_block = block_tables[(int64_t)b * bt_stride + nblocks - 1];
+        const int32_t last_block_num_tokens = len - (nblocks - 1) * block_size;
+        context_lens[b] = len;
+        positions[b] = len - 1;
+        slot_mapping[b] = last_block * block_size + last_block_num_tokens - 1;
+    }
+    return bad;
+}
+
+/* Field guide Step 07.5 "prepare_prefill: pack a varlen batch": sequence b schedules the new
+ * tokens [start, end) with start = num_cached[b], end = start + num_scheduled[b]; their positions
+ * are start .. end-1; cu_seqlens_q accumulates num_scheduled, cu_seqlens_k accumulates end (the
+ * keys include the cached prefix); max_seqlens = {max seqlen_q, max seqlen_k}; slot_mapping walks
+ * the blocks the range touches: the first starts at start % block_size, the last ends at
+ * end - i * block_size, the ones between contribute all their slots.  Returns the number of
+ * tokens written (the sum of num_scheduled), or -1 when a range needs a block the table lacks. */
+int64_t oracle_prepare_prefill(const int32_t *num_cached, const int32_t *num_scheduled, const int32_t *block_tables,
+                               int32_t bt_stride, int32_t num_seqs, int32_t block_size, int32_t *cu_seqlens_q,
+                               int32_t *cu_seqlens_k, int32_t *positions, int32_t *slot_mapping,
+                               int32_t *max_seqlens)
+{
+    int64_t n = 0;
+    cu_seqlens_q[0] = 0;
+    cu_seqlens_k[0] = 0;
+    max_seqlens[0] = 0;
+    max_seqlens[1] = 0;
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        const int32_t start = num_cached[b];
+        const int32_t seqlen_q = num_scheduled[b];
+        const int32_t end = start + seqlen_q;
+        cu_seqlens_q[b + 1] = cu_seqlens_q[b] + seqlen_q;
+        cu_seqlens_k[b + 1] = cu_seqlens_k[b] + end;
+        if (seqlen_q > max_seqlens[0])
+            max_seqlens[0] = seqlen_q;
+        if (end > max_seqlens[1])
+            max_seqlens[1] = end;
+        for (int32_t p = start; p < end; ++p)
+            positions[n + (p - start)] = p;
+        const int32_t start_block = start / block_size;
+        const int32_t end_block = (end + block_size - 1) / block_size;
+        if (end_block > bt_stride)
+            return -1;
+        int64_t k = n;
+        for (int32_t i = start_block; i < end_block; ++i) {
+            const int32_t base = block_tables[(int64_t)b * bt_stride + i] * block_size;
+            const int32_t slot_start = base + (i == start_block ? start % block_size : 0);
+            const int32_t slot_end = (i != end_block - 1) ? base + block_size : base + end - i * block_size;
+            for (int32_t s = slot_start; s < slot_end; ++s)
+                slot_mapping[k++] = s;
+        }
+        n += seqlen_q;
+    }
+    return n;
+}

@@ -414,7 +414,91 @@ def check_prologue_zero_vector_and_slots(orc):
     assert np.array_equal(vc[1], qkv[3, (hq + hkv) * d:])
 
 
+# ---------------------------------------------------------------------------
+# attention metadata: prepare_decode / prepare_prefill (worked examples on the pages)
+# ---------------------------------------------------------------------------
+
+def check_prepare_decode_golden(orc):
+    for ex in golden()["decode"]:
+        tables = [s["block_table"] for s in ex["seqs"]]
+        w = ex.get("block_table_width", max(len(t) for t in tables))
+        bt = np.full((len(tables), w), -1, np.int32)
+        for i, t in enumerate(tables):
+            bt[i, :len(t)] = t
+        lens = [s["num_tokens"] for s in ex["seqs"]]
+        pad = ex.get("bucket", len(lens))
+        cl, pos, sm, bad = orc.prepare_decode(lens, bt, ex["block_size"], pad)
+        assert bad == 0
+        assert cl[:len(lens)].tolist() == ex["context_lens"], ex["cite"]
+        assert pos[:len(lens)].tolist() == ex["positions"], ex["cite"]
+        if "slot_mapping" in ex:
+            assert sm[:len(lens)].tolist() == ex["slot_mapping"], ex["cite"]
+        for i, L in enumerate(lens):          # the slot of position L-1, by the single-position rule
+            assert sm[i] == orc.slot_of(tables[i], L - 1, ex["block_size"])
+        if "bucket" in ex:
+            assert (sm[len(lens):] == ex["bucket_slot_pad"]).all() and (cl[len(lens):] == ex["bucket_context_pad"]).all()
+
+
+def check_prepare_prefill_golden(orc):
+    for ex in golden()["prefill"]:
+        tables = [s["block_table"] for s in ex["seqs"]]
+        w = max(len(t) for t in tables)
+        bt = np.full((len(tables), w), -1, np.int32)
+        for i, t in enumerate(tables):
+            bt[i, :len(t)] = t
+        nc = [s["num_cached_tokens"] for s in ex["seqs"]]
+        ns = [s["num_scheduled_tokens"] for s in ex["seqs"]]
+        cq, ck, pos, sm, mx = orc.prepare_prefill(nc, ns, bt, ex["block_size"])
+        assert cq.tolist() == ex["cu_seqlens_q"] and ck.tolist() == ex["cu_seqlens_k"], ex["cite"]
+        assert mx == (ex["max_seqlen_q"], ex["max_seqlen_k"]), ex["cite"]
+        if "positions" in ex:
+            assert pos.tolist() == ex["positions"], ex["cite"]
+        if "slot_mapping" in ex:
+            assert sm.tolist() == ex["slot_mapping"], ex["cite"]
+        # every token's slot is the slot of its position, by the single-position rule
+        t = 0
+        for b in range(len(tables)):
+            for p_ in range(nc[b], nc[b] + ns[b]):
+                assert sm[t] == orc.slot_of(tables[b], p_, ex["block_size"])
+                t += 1
+
+
+def check_prepare_random_consistency(orc):
+    """Random batches: decode slots are the slots of position L-1, prefill slots of each position;
+    a row whose length needs more blocks than its table holds is rejected."""
+    rng = np.random.default_rng(9)
+    for bs in (4, 16, 256):
+        lens = rng.integers(1, 40 * bs // 16 + 2, 12)
+        nb = (lens + bs - 1) // bs
+        bt = np.full((12, int(nb.max())), -1, np.int32)
+        perm = rng.permutation(int(nb.sum()))
+        k = 0
+        for i, n in enumerate(nb):
+            bt[i, :n] = perm[k:k + n]
+            k += n
+        cl, pos, sm, bad = orc.prepare_decode(lens, bt, bs, 15)
+        assert bad == 0 and (cl[:12] == lens).all() and (pos[:12] == lens - 1).all()
+        for i in range(12):
+            assert sm[i] == orc.slot_of(bt[i], int(lens[i]) - 1, bs)
+        assert (sm[12:] == -1).all() and (cl[12:] == 0).all()
+        cached = (rng.random(12) * lens).astype(np.int32)
+        sched = (lens - cached).astype(np.int32)
+        cq, ck, pos, sm, mx = orc.prepare_prefill(cached, sched, bt, bs)
+        assert ck[-1] == lens.sum() and cq[-1] == sched.sum()
+        t = 0
+        for i in range(12):
+            for p_ in range(int(cached[i]), int(lens[i])):
+                assert pos[t] == p_ and sm[t] == orc.slot_of(bt[i], p_, bs)
+                t += 1
+        too_long = lens.copy()
+        too_long[3] = bt.shape[1] * bs + 1
+        assert orc.prepare_decode(too_long, bt, bs)[3] == 1
+
+
 ALL_CHECKS = [
+    check_prepare_decode_golden,
+    check_prepare_prefill_golden,
+    check_prepare_random_consistency,
     check_prologue_brute_force,
     check_prologue_position_zero_is_norm_only,
     check_prologue_rope_closed_form,

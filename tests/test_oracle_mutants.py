@@ -39,6 +39,16 @@ MUTANTS = {
     "k_normed_with_q_weight": ("norm_rope_head(krow + (int64_t)h * head_dim, k_weight,",
                                "norm_rope_head(krow + (int64_t)h * head_dim, q_weight,"),
     "v_stored_from_k": ("memcpy(v_cache + slot * dkv, vrow,", "memcpy(v_cache + slot * dkv, krow,"),
+    # attention metadata
+    "decode_slot_one_past": ("slot_mapping[b] = last_block * block_size + last_block_num_tokens - 1;",
+                             "slot_mapping[b] = last_block * block_size + last_block_num_tokens;"),
+    "decode_position_is_len": ("positions[b] = len - 1;", "positions[b] = len;"),
+    "decode_padding_not_cleared": ("        slot_mapping[b] = -1;\n        if (b >= num_seqs)",
+                                   "        slot_mapping[b] = 0;\n        if (b >= num_seqs)"),
+    "prefill_cu_k_counts_new_tokens": ("cu_seqlens_k[b + 1] = cu_seqlens_k[b] + end;",
+                                       "cu_seqlens_k[b + 1] = cu_seqlens_k[b] + seqlen_q;"),
+    "prefill_first_block_offset_dropped": ("(i == start_block ? start % block_size : 0)", "0"),
+    "prefill_positions_from_zero": ("positions[n + (p - start)] = p;", "positions[n + (p - start)] = p - start;"),
 }
 
 _RUNNER = r"""
