@@ -305,6 +305,42 @@ def run_ours(args, rank, world, local_rank):
         fused_ms = f0.elapsed_time(f1)
         assert int(d_err.item()) == 0, f"device error flags {int(d_err.item())}"
 
+        # device-side attention metadata for the same decode batch (NEXT-3) against the pages' host path
+        pd_out = tuple(torch.empty(db.num_seqs, dtype=torch.int32, device=dev) for _ in range(3))
+        for _ in range(args.warmup):
+            nv.nv_prepare_decode(ctx, bt, db.block_size, db.num_blocks, out=pd_out, d_err=d_err)
+        # captured in a CUDA graph so the number is device time, not the binding's launch rate
+        g_meta = torch.cuda.CUDAGraph()
+        cap_stream = torch.cuda.Stream()
+        cap_stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap_stream):
+            with torch.cuda.graph(g_meta, stream=cap_stream):
+                for _ in range(20):
+                    nv.nv_prepare_decode(ctx, bt, db.block_size, db.num_blocks, out=pd_out, d_err=d_err)
+        torch.cuda.current_stream().wait_stream(cap_stream)
+        g_meta.replay()
+        m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(1, args.steps // 20)
+        m0.record(stream)
+        for _ in range(reps):
+            g_meta.replay()
+        m1.record(stream)
+        torch.cuda.synchronize()
+        meta_dev_us = m0.elapsed_time(m1) * 1e3 / (reps * 20)
+        assert torch.equal(pd_out[2].cpu(), torch.from_numpy(db.slot_mapping)), "device slots differ"
+        from paged_kv_attention_store_gb300 import metadata as host_meta
+        seqs_host = [(db.block_tables[i][db.block_tables[i] >= 0].tolist(), int(db.seq_lens[i]))
+                     for i in range(db.num_seqs)]
+        host_steps = max(5, min(args.steps, 50))
+        torch.cuda.synchronize()
+        t_h = time.perf_counter()
+        for _ in range(host_steps):
+            hm = host_meta.prepare_decode(seqs_host, db.block_size, width=db.block_tables.shape[1])
+            for arr in (hm.positions, hm.slot_mapping, hm.context_lens, hm.block_tables):
+                torch.from_numpy(arr).pin_memory().to(dev, non_blocking=True)
+        torch.cuda.synchronize()
+        meta_host_us = (time.perf_counter() - t_h) * 1e6 / host_steps
+
         # ---------------- prefill phase: store + prefill on the chunked-prefill batch ----------------
         del k_cache, v_cache, ws
         torch.cuda.empty_cache()
@@ -444,10 +480,20 @@ def run_ours(args, rank, world, local_rank):
             "note": "same step as the headline (store 512 rows + decode) in one pass: the new rows are read once "
                     "from the inputs and written to the pool by the decode kernel",
         },
-        "gpu_launches": (launches_per_decode_step * 2 + (launches_per_decode_step - 1) + 3 + 1) * args.steps,
-        "gpu_launches_note": "decode phase: store + split-KV decode + merge per step; e2e phase: same kernels; "
-                             "fused phase: fused decode + merge; prefill phase: store + work-list pre-pass + prefill; "
-                             "prologue phase: one kernel per step",
+        "prepare_decode": {
+            "kernel": "prepare_decode_kernel (nv_prepare_decode)", "rows": db.num_seqs,
+            "device_us_per_call": round(meta_dev_us, 2),
+            "device_timing": "20 calls captured in a CUDA graph, replayed; CUDA events around the replays",
+            "host_path_us_per_step": round(meta_host_us, 1),
+            "note": "the pages build positions / slot_mapping / context_lens / block tables in Python each decode step "
+                    "and copy them from pinned memory; the device call derives the first three from lengths and "
+                    "tables already on the GPU (slots checked equal to the host-built ones)",
+        },
+        "gpu_launches": launches_per_decode_step * args.steps,
+        "gpu_launches_note": "kernels of this library launched in the headline timed region (store + split-KV decode "
+                             "+ merge per step); all timed phases together: see gpu_launches_all_phases",
+        "gpu_launches_all_phases": (launches_per_decode_step * 2 + (launches_per_decode_step - 1) + 1 + 3 + 1)
+                                   * args.steps,
         "clocks": clocks,
         "prefill": {
             "workload": "chunked prefill with prefix cache (store 16384 new rows + causal varlen prefill): 16 seqs, "

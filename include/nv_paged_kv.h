@@ -119,6 +119,41 @@ int nv_qk_norm_rope_store(const void *qkv, int64_t qkv_row_stride, const int32_t
                           int32_t *d_err, nv_stream_t stream);
 
 /*
+ * nv_prepare_decode -- a decode step's attention metadata, built on the device.
+ *
+ * Field guide Step 07.6 "prepare_decode" and Step 07.8 (graph-replay padding): for sequence b with
+ * len = seq_lens[b] tokens (the new one included): context_lens[b] = len, positions[b] = len - 1,
+ * slot_mapping[b] = the slot of position len - 1 (the last block's base slot plus
+ * last_block_num_tokens - 1).  Rows num_seqs .. padded_seqs-1 get slot -1, context 0 and position 0,
+ * so a graph replayed at a larger bucket stores and attends to nothing for them.  A row whose length
+ * is < 1 or needs more blocks than bt_stride (NV_DERR_LENGTH), or whose last block id lies outside
+ * [0, num_blocks) (NV_DERR_BLOCK_RANGE), is written as a padding row.
+ *   seq_lens int32 [num_seqs]; block_tables int32 [num_seqs, bt_stride]; outputs int32 [padded_seqs].
+ *   block_size a power of two; num_blocks * block_size < 2^31.
+ */
+int nv_prepare_decode(const int32_t *seq_lens, const int32_t *block_tables, int32_t bt_stride, int32_t num_seqs,
+                      int32_t padded_seqs, int32_t block_size, int32_t num_blocks, int32_t *context_lens,
+                      int32_t *positions, int32_t *slot_mapping, int32_t *d_err, nv_stream_t stream);
+
+/*
+ * nv_prepare_prefill -- a prefill step's attention metadata, built on the device.
+ *
+ * Field guide Step 07.5 "prepare_prefill": sequence b schedules positions [start, end) with
+ * start = num_cached[b], end = start + num_scheduled[b].  Writes cu_seqlens_q ([num_seqs + 1],
+ * running sum of num_scheduled), cu_seqlens_k ([num_seqs + 1], running sum of end: the keys include
+ * the cached prefix), max_seqlens ([2]: max num_scheduled, max end), and for every new token t (packed
+ * in sequence order) positions[t] and slot_mapping[t] = the slot of that position through the
+ * sequence's block table.  total_q is the host's count of new tokens (the scheduler knows it): the
+ * outputs positions / slot_mapping have total_q entries; if the lengths add up to a different total,
+ * NV_DERR_LENGTH is set and only the first min of the two are meaningful.  Tokens whose block is
+ * missing or out of range get slot -1 (NV_DERR_LENGTH / NV_DERR_BLOCK_RANGE).  Two launches.
+ */
+int nv_prepare_prefill(const int32_t *num_cached, const int32_t *num_scheduled, const int32_t *block_tables,
+                       int32_t bt_stride, int32_t num_seqs, int32_t total_q, int32_t block_size, int32_t num_blocks,
+                       int32_t *cu_seqlens_q, int32_t *cu_seqlens_k, int32_t *positions, int32_t *slot_mapping,
+                       int32_t *max_seqlens, int32_t *d_err, nv_stream_t stream);
+
+/*
  * Bytes of workspace nv_paged_decode_attn needs for this batch (0 means none).  Depends only
  * on its arguments, so it can be sized once for the largest batch and reused.
  */

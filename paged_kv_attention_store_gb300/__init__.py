@@ -31,7 +31,7 @@ NV_DERR_SLOT_MISMATCH = 0x10
 
 EXPORTED = ("nv_status_string", "nv_store_kvcache", "nv_paged_decode_workspace_size", "nv_paged_decode_attn",
             "nv_store_decode_attn", "nv_paged_decode_attn_noalloc", "nv_paged_prefill_workspace_size",
-            "nv_paged_prefill_attn", "nv_qk_norm_rope_store")
+            "nv_paged_prefill_attn", "nv_qk_norm_rope_store", "nv_prepare_decode", "nv_prepare_prefill")
 
 
 class NvError(RuntimeError):
@@ -65,6 +65,10 @@ def load_library(path: str | None = None):
     L.nv_paged_decode_workspace_size.restype = sz
     L.nv_paged_decode_attn.argtypes = [V, V, V, V, i32, V, i32, i32, i32, i32, i32, i32, i32, f32, V, V, sz, V, V]
     L.nv_paged_decode_attn.restype = ctypes.c_int
+    L.nv_prepare_decode.argtypes = [V, V, i32, i32, i32, i32, i32, V, V, V, V, V]
+    L.nv_prepare_decode.restype = ctypes.c_int
+    L.nv_prepare_prefill.argtypes = [V, V, V, i32, i32, i32, i32, i32, V, V, V, V, V, V, V]
+    L.nv_prepare_prefill.restype = ctypes.c_int
     L.nv_qk_norm_rope_store.argtypes = [V, i64, V, V, V, f32, f32, V, i32, i32, i32, i32, V, V, V, i64, V, V]
     L.nv_qk_norm_rope_store.restype = ctypes.c_int
     L.nv_store_decode_attn.argtypes = [V, V, i64, V, i64, V, V, V, V, i32, V, i32, i32, i32, i32, i32, i32, i32, f32,
@@ -122,6 +126,44 @@ def nv_store_kvcache(k, v, slot_mapping, k_cache, v_cache, d_err=None, stream=No
     rc = load_library().nv_store_kvcache(_ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(slot_mapping), n,
                                          _ptr(k_cache), _ptr(v_cache), nb * bs, hkv, d, _ptr(d_err), _stream(stream))
     _check("nv_store_kvcache", rc)
+
+
+def nv_prepare_decode(seq_lens, block_tables, block_size, num_blocks, padded_seqs=None, out=None, d_err=None,
+                      stream=None):
+    """Device-side decode metadata: returns ``(context_lens, positions, slot_mapping)`` int32 ``[padded]``
+    for sequences of ``seq_lens`` tokens (new token included) over ``block_tables``."""
+    import torch
+    B = int(seq_lens.shape[0])
+    pad = B if padded_seqs is None else int(padded_seqs)
+    _need(block_tables.dim() == 2 and block_tables.shape[0] >= B and block_tables.stride(1) == 1,
+          "block_tables must be [B, W] with unit column stride")
+    if out is None:
+        out = tuple(torch.empty(pad, dtype=torch.int32, device=seq_lens.device) for _ in range(3))
+    cl, pos, sm = out
+    rc = load_library().nv_prepare_decode(_ptr(seq_lens), _ptr(block_tables), block_tables.stride(0), B, pad,
+                                          int(block_size), int(num_blocks), _ptr(cl), _ptr(pos), _ptr(sm), _ptr(d_err),
+                                          _stream(stream))
+    _check("nv_prepare_decode", rc)
+    return cl, pos, sm
+
+
+def nv_prepare_prefill(num_cached, num_scheduled, block_tables, block_size, num_blocks, total_q, d_err=None,
+                       stream=None):
+    """Device-side prefill metadata: returns ``(cu_seqlens_q, cu_seqlens_k, positions, slot_mapping, max_seqlens)``."""
+    import torch
+    B = int(num_cached.shape[0])
+    dev = num_cached.device
+    cq = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    ck = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    pos = torch.empty(max(int(total_q), 1), dtype=torch.int32, device=dev)
+    sm = torch.empty(max(int(total_q), 1), dtype=torch.int32, device=dev)
+    mx = torch.empty(2, dtype=torch.int32, device=dev)
+    rc = load_library().nv_prepare_prefill(_ptr(num_cached), _ptr(num_scheduled), _ptr(block_tables),
+                                           block_tables.stride(0), B, int(total_q), int(block_size), int(num_blocks),
+                                           _ptr(cq), _ptr(ck), _ptr(pos), _ptr(sm), _ptr(mx), _ptr(d_err),
+                                           _stream(stream))
+    _check("nv_prepare_prefill", rc)
+    return cq, ck, pos[:int(total_q)], sm[:int(total_q)], mx
 
 
 def nv_qk_norm_rope_store(qkv, positions, q_norm_weight, k_norm_weight, slot_mapping, k_cache, v_cache,

@@ -122,6 +122,17 @@ def test_prologue_validation(lib):
     assert _prologue(lib, eps=-1.0) == NV_ERR_SHAPE
 
 
+def test_prepare_validation(lib):
+    assert lib.nv_prepare_decode(FAKE, FAKE, 4, 0, 0, 256, 8, FAKE, FAKE, FAKE, None, None) == 0
+    assert lib.nv_prepare_decode(FAKE, FAKE, 4, 3, 2, 256, 8, FAKE, FAKE, FAKE, None, None) == NV_ERR_SHAPE  # pad < n
+    assert lib.nv_prepare_decode(None, FAKE, 4, 3, 3, 256, 8, FAKE, FAKE, FAKE, None, None) == NV_ERR_NULL
+    assert lib.nv_prepare_decode(FAKE, FAKE, 4, 3, 3, 48, 8, FAKE, FAKE, FAKE, None, None) == NV_ERR_UNSUPPORTED
+    assert lib.nv_prepare_prefill(FAKE, FAKE, FAKE, 4, 0, 0, 256, 8, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == 0
+    assert lib.nv_prepare_prefill(FAKE, None, FAKE, 4, 2, 5, 256, 8, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == NV_ERR_NULL
+    assert lib.nv_prepare_prefill(FAKE, FAKE, FAKE, 4, 2, 5, 100, 8, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                                  None) == NV_ERR_UNSUPPORTED
+
+
 def _prefill(lib, q=FAKE, kc=FAKE, vc=FAKE, cq=FAKE, ck=FAKE, bt=FAKE, bts=8, B=2, tq=100, mq=80, hq=16, hkv=8,
              d=128, bs=256, nb=16, out=FAKE, ws=FAKE, wsb=256):
     return lib.nv_paged_prefill_attn(q, kc, vc, cq, ck, bt, bts, B, tq, mq, hq, hkv, d, bs, nb, 0.088, out, ws, wsb,
