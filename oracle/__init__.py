@@ -65,6 +65,8 @@ def _load(path: str):
     L.oracle_prepare_decode.restype = i64
     L.oracle_prepare_prefill.argtypes = [P, P, P, i32, i32, i32, P, P, P, P, P]
     L.oracle_prepare_prefill.restype = i64
+    L.oracle_sample_exponential_race.argtypes = [P, i64, P, P, i64, i32, i32, P]
+    L.oracle_sample_exponential_race.restype = None
     return L
 
 
@@ -222,6 +224,23 @@ class Oracle:
                                             _ptr(ck), _ptr(pos), _ptr(sm), _ptr(mx))
         assert n == total, n
         return cq, ck, pos[:total], sm[:total], (int(mx[0]), int(mx[1]))
+
+    def sample(self, logits, temperatures, draws, threads: int = 1):
+        """int64 ``[B]``: argmax_i softmax(logits/T)_i / max(E_i, 1e-10) per row (first index on ties)."""
+        lg = _c(logits, np.uint16)
+        ex = _c(draws, np.float32)
+        tm = _c(temperatures, np.float32)
+        B, V = lg.shape
+        out = np.zeros(B, np.int64)
+
+        def run(lo, hi):
+            sub = np.zeros(hi - lo, np.int64)
+            self.lib.oracle_sample_exponential_race(_ptr(lg[lo:hi]), V, _ptr(tm[lo:hi]), _ptr(ex[lo:hi]), V, hi - lo,
+                                                    V, _ptr(sub))
+            out[lo:hi] = sub
+
+        _parallel(run, B, threads)
+        return out
 
 
 def slot_of(table, pos, block_size):

@@ -361,3 +361,47 @@ int64_t oracle_prepare_prefill(const int32_t *num_cached, const int32_t *num_sch
     }
     return n;
 }
+
+/* ------------------------------------------------------------------------------------
+ * Sampler: temperature and the exponential race.
+ *
+ * Field guide, "sampler.py": logits (bf16, widened to float32) are divided by the row's temperature
+ * and turned into probabilities with softmax; the sampled token is argmax_i p_i / E_i, where the
+ * E_i are independent Exp(1) draws clamped below at 1e-10.  Here the draws are an input (the pages
+ * draw them with torch's exponential_).  The argmax takes the first index on ties (torch's argmax
+ * returns the first occurrence).  float32 throughout, as the pages compute it.
+ * ------------------------------------------------------------------------------------ */
+void oracle_sample_exponential_race(const uint16_t *logits, int64_t logits_stride, const float *temperatures,
+                                    const float *draws, int64_t draws_stride, int32_t num_rows, int32_t vocab,
+                                    int64_t *tokens)
+{
+    float *p = (float *)malloc(sizeof(float) * (size_t)vocab);
+    for (int32_t r = 0; r < num_rows; ++r) {
+        const uint16_t *lr = logits + (int64_t)r * logits_stride;
+        const float *er = draws + (int64_t)r * draws_stride;
+        const float t = temperatures[r];
+        float m = -INFINITY;
+        for (int32_t i = 0; i < vocab; ++i) {
+            p[i] = widen_bf16(lr[i]) / t;
+            if (p[i] > m)
+                m = p[i];
+        }
+        float sum = 0.0f;
+        for (int32_t i = 0; i < vocab; ++i) {
+            p[i] = expf(p[i] - m);
+            sum += p[i];
+        }
+        int64_t best = 0;
+        float best_v = -INFINITY;
+        for (int32_t i = 0; i < vocab; ++i) {
+            const float e = er[i] < 1e-10f ? 1e-10f : er[i];
+            const float v = (p[i] / sum) / e;
+            if (v > best_v) {
+                best_v = v;
+                best = i;
+            }
+        }
+        tokens[r] = best;
+    }
+    free(p);
+}

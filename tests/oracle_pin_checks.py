@@ -495,7 +495,68 @@ def check_prepare_random_consistency(orc):
         assert orc.prepare_decode(too_long, bt, bs)[3] == 1
 
 
+# ---------------------------------------------------------------------------
+# sampler: temperature and the exponential race
+# ---------------------------------------------------------------------------
+
+def _logit_bits(vals):
+    return W.f32_to_bf16_bits(np.asarray(vals, np.float32))
+
+
+def check_sampler_unit_draws_is_greedy(orc):
+    """With every draw equal to 1 the race is won by the most probable token: the first argmax of the
+    logits, whatever the temperature."""
+    rng = np.random.default_rng(11)
+    lg = _logit_bits(rng.standard_normal((6, 1000)) * 3)
+    lg[2, 5] = lg[2, 700] = _logit_bits([30.0])[0]           # a tie: the first index wins
+    want = np.argmax(brute.widen(lg), axis=1)
+    for t in (0.3, 1.0, 2.5):
+        got = orc.sample(lg, np.full(6, t, np.float32), np.ones((6, 1000), np.float32))
+        assert np.array_equal(got, want), (t, got, want)
+    assert want[2] == 5
+
+
+def check_sampler_closed_form(orc):
+    """logits [2, 0], draws [1, 0.2]: p = softmax([2, 0] / T); p0 / 1 vs p1 / 0.2 -- token 0 at T = 1
+    (0.881 vs 0.596), token 1 at T = 4 (0.622 vs 1.89).  Equal logits: the smallest draw wins."""
+    lg = _logit_bits([[2.0, 0.0]])
+    e = np.array([[1.0, 0.2]], np.float32)
+    assert orc.sample(lg, np.array([1.0], np.float32), e)[0] == 0
+    assert orc.sample(lg, np.array([4.0], np.float32), e)[0] == 1
+    eq = _logit_bits(np.zeros((1, 9)))
+    d = np.array([[3.0, 0.5, 2.0, 0.4, 0.9, 0.4, 7.0, 1.0, 0.41]], np.float32)
+    assert orc.sample(eq, np.array([0.8], np.float32), d)[0] == 3
+
+
+def check_sampler_large_logits_finite(orc):
+    """Logits of 100 at temperature 0.5 (scores of 200) still sample the right token (the softmax is
+    max-subtracted)."""
+    lg = _logit_bits([[100.0, 99.0, 90.0]])
+    d = np.array([[1.0, 0.1, 1.0]], np.float32)          # p1/p0 = e^-2 = 0.135 > 0.1: token 1 wins
+    assert orc.sample(lg, np.array([0.5], np.float32), d)[0] == 1
+
+
+def check_sampler_distribution(orc):
+    """The race picks token i with probability softmax(l / T)_i: empirical frequencies over 40000
+    independent draws agree within 5 standard errors."""
+    lg = _logit_bits([[1.0, 0.5, -0.3, 2.0, 0.0, -1.5, 1.2, 0.8]])
+    t = 0.7
+    rng = np.random.default_rng(12)
+    n = 40000
+    draws = rng.exponential(1.0, (n, 8)).astype(np.float32)
+    tok = orc.sample(np.repeat(lg, n, axis=0), np.full(n, t, np.float32), draws, threads=4)
+    p = np.exp(brute.widen(lg[0]) / t)
+    p /= p.sum()
+    freq = np.bincount(tok, minlength=8) / n
+    se = np.sqrt(p * (1 - p) / n)
+    assert (np.abs(freq - p) < 5 * se + 1e-12).all(), (freq, p)
+
+
 ALL_CHECKS = [
+    check_sampler_unit_draws_is_greedy,
+    check_sampler_closed_form,
+    check_sampler_large_logits_finite,
+    check_sampler_distribution,
     check_prepare_decode_golden,
     check_prepare_prefill_golden,
     check_prepare_random_consistency,

@@ -49,6 +49,12 @@ MUTANTS = {
                                        "cu_seqlens_k[b + 1] = cu_seqlens_k[b] + seqlen_q;"),
     "prefill_first_block_offset_dropped": ("(i == start_block ? start % block_size : 0)", "0"),
     "prefill_positions_from_zero": ("positions[n + (p - start)] = p;", "positions[n + (p - start)] = p - start;"),
+    # sampler
+    "sampler_temperature_multiplies": ("p[i] = widen_bf16(lr[i]) / t;", "p[i] = widen_bf16(lr[i]) * t;"),
+    "sampler_draw_multiplies": ("const float v = (p[i] / sum) / e;", "const float v = (p[i] / sum) * e;"),
+    "sampler_last_index_on_ties": ("if (v > best_v) {", "if (v >= best_v) {"),
+    "sampler_no_max_subtraction": ("p[i] = expf(p[i] - m);", "p[i] = expf(p[i]);"),
+    "sampler_draws_ignored": ("const float v = (p[i] / sum) / e;", "const float v = (p[i] / sum);"),
 }
 
 _RUNNER = r"""
