@@ -341,6 +341,29 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         meta_host_us = (time.perf_counter() - t_h) * 1e6 / host_steps
 
+        # sampler (exponential race) over the decode batch's rows and the Qwen3 vocabulary
+        V_SAMPLE = 151936
+        srng = np.random.default_rng([rank, 17])
+        s_logits = to_dev(W.f32_to_bf16_bits((srng.standard_normal((db.num_seqs, V_SAMPLE)) * 3.0)
+                                             .astype(np.float32)))
+        s_temps = torch.from_numpy(srng.uniform(0.5, 1.5, db.num_seqs).astype(np.float32)).to(dev)
+        s_draws = torch.from_numpy(srng.exponential(1.0, (db.num_seqs, V_SAMPLE)).astype(np.float32)).to(dev)
+        s_tok = torch.empty(db.num_seqs, dtype=torch.int64, device=dev)
+        s_ws = torch.empty(max(nv.load_library().nv_sample_workspace_size(db.num_seqs, V_SAMPLE), 16),
+                           dtype=torch.uint8, device=dev)
+        for _ in range(args.warmup):
+            nv.nv_sample_exponential_race(s_logits, s_temps, s_draws, tokens=s_tok, workspace=s_ws, d_err=d_err)
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.steps):
+            nv.nv_sample_exponential_race(s_logits, s_temps, s_draws, tokens=s_tok, workspace=s_ws, d_err=d_err)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        sample_ms = s0.elapsed_time(s1) / args.steps
+        sample_bytes = db.num_seqs * V_SAMPLE * (2 + 4) + db.num_seqs * (4 + 8)
+        del s_logits, s_draws
+        assert int(d_err.item()) == 0, f"device error flags {int(d_err.item())}"
+
         # ---------------- prefill phase: store + prefill on the chunked-prefill batch ----------------
         del k_cache, v_cache, ws
         torch.cuda.empty_cache()
@@ -489,10 +512,20 @@ def run_ours(args, rank, world, local_rank):
                     "and copy them from pinned memory; the device call derives the first three from lengths and "
                     "tables already on the GPU (slots checked equal to the host-built ones)",
         },
+        "sampler": {
+            "kernel": "sample_partial_kernel + sample_merge_kernel (nv_sample_exponential_race)",
+            "workload": f"{db.num_seqs} rows x 151936-entry vocabulary: bf16 logits N(0, 9), T ~ U[0.5, 1.5], "
+                        "float32 Exp(1) draws; inputs (467 MB) larger than L2",
+            "ms": round(sample_ms, 4),
+            "roofline": {"bound": "hbm", "achieved": round(sample_bytes / (sample_ms * 1e-3) / 1e9, 1),
+                         "peak": float(pk["hbm_gbs"]), "unit": "GB/s",
+                         "frac": round(sample_bytes / (sample_ms * 1e-3) / 1e9 / float(pk["hbm_gbs"]), 4),
+                         "algorithmic_bytes_per_launch": sample_bytes},
+        },
         "gpu_launches": launches_per_decode_step * args.steps,
         "gpu_launches_note": "kernels of this library launched in the headline timed region (store + split-KV decode "
                              "+ merge per step); all timed phases together: see gpu_launches_all_phases",
-        "gpu_launches_all_phases": (launches_per_decode_step * 2 + (launches_per_decode_step - 1) + 1 + 3 + 1)
+        "gpu_launches_all_phases": (launches_per_decode_step * 2 + (launches_per_decode_step - 1) + 1 + 2 + 3 + 1)
                                    * args.steps,
         "clocks": clocks,
         "prefill": {

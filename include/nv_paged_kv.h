@@ -61,6 +61,7 @@ typedef enum nv_status {
 #define NV_DERR_LENGTH 0x4        /* a length exceeds the block table, the host hint, or is negative */
 #define NV_DERR_TIMEOUT 0x8       /* a bounded wait on an asynchronous copy gave up */
 #define NV_DERR_SLOT_MISMATCH 0x10 /* fused store + decode: a slot that is not position L-1's (row not stored) */
+#define NV_DERR_VALUE 0x20         /* sampler: a temperature that is not positive and finite (token -1) */
 
 /* Human-readable name of an nv_status value (static string). */
 const char *nv_status_string(int status);
@@ -152,6 +153,29 @@ int nv_prepare_prefill(const int32_t *num_cached, const int32_t *num_scheduled, 
                        int32_t bt_stride, int32_t num_seqs, int32_t total_q, int32_t block_size, int32_t num_blocks,
                        int32_t *cu_seqlens_q, int32_t *cu_seqlens_k, int32_t *positions, int32_t *slot_mapping,
                        int32_t *max_seqlens, int32_t *d_err, nv_stream_t stream);
+
+/*
+ * nv_sample_exponential_race -- temperature sampling by the exponential race.
+ *
+ * Field guide, "sampler.py: temperature and the exponential race": logits are divided by each row's
+ * temperature and turned into probabilities with softmax; the token is argmax_i p_i / E_i, where the
+ * E_i are independent Exp(1) draws clamped below at 1e-10 -- token i wins with probability p_i.  The
+ * draws are an input (the pages draw them with torch's exponential_); the first index wins a tie.
+ *   logits        bf16 [num_rows, logits_stride] (first vocab entries used; stride a multiple of 8).
+ *   temperatures  float32 [num_rows], each > 0 and finite (else the row's token is -1 and
+ *                 NV_DERR_VALUE is set).
+ *   draws         float32 [num_rows, draws_stride] (stride a multiple of 4).  Both bases 16-byte aligned.
+ *   tokens        int64 [num_rows] (out).
+ *   workspace     at least nv_sample_workspace_size(num_rows, vocab) bytes, 16-byte aligned.
+ * The argmax is taken over logits_i * log2(e) / T - log2(max(E_i, 1e-10)), which orders the
+ * entries exactly as p_i / E_i does; rounding can only matter between entries within a few
+ * float32 ulps of each other.  Two launches.
+ */
+size_t nv_sample_workspace_size(int32_t num_rows, int32_t vocab);
+
+int nv_sample_exponential_race(const void *logits, int64_t logits_stride, const float *temperatures, const float *draws,
+                               int64_t draws_stride, int32_t num_rows, int32_t vocab, int64_t *tokens, void *workspace,
+                               size_t workspace_bytes, int32_t *d_err, nv_stream_t stream);
 
 /*
  * Bytes of workspace nv_paged_decode_attn needs for this batch (0 means none).  Depends only

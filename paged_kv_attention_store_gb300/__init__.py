@@ -28,10 +28,12 @@ NV_DERR_BLOCK_RANGE = 0x2
 NV_DERR_LENGTH = 0x4
 NV_DERR_TIMEOUT = 0x8
 NV_DERR_SLOT_MISMATCH = 0x10
+NV_DERR_VALUE = 0x20
 
 EXPORTED = ("nv_status_string", "nv_store_kvcache", "nv_paged_decode_workspace_size", "nv_paged_decode_attn",
             "nv_store_decode_attn", "nv_paged_decode_attn_noalloc", "nv_paged_prefill_workspace_size",
-            "nv_paged_prefill_attn", "nv_qk_norm_rope_store", "nv_prepare_decode", "nv_prepare_prefill")
+            "nv_paged_prefill_attn", "nv_qk_norm_rope_store", "nv_prepare_decode", "nv_prepare_prefill",
+            "nv_sample_workspace_size", "nv_sample_exponential_race")
 
 
 class NvError(RuntimeError):
@@ -65,6 +67,10 @@ def load_library(path: str | None = None):
     L.nv_paged_decode_workspace_size.restype = sz
     L.nv_paged_decode_attn.argtypes = [V, V, V, V, i32, V, i32, i32, i32, i32, i32, i32, i32, f32, V, V, sz, V, V]
     L.nv_paged_decode_attn.restype = ctypes.c_int
+    L.nv_sample_workspace_size.argtypes = [i32, i32]
+    L.nv_sample_workspace_size.restype = sz
+    L.nv_sample_exponential_race.argtypes = [V, i64, V, V, i64, i32, i32, V, V, sz, V, V]
+    L.nv_sample_exponential_race.restype = ctypes.c_int
     L.nv_prepare_decode.argtypes = [V, V, i32, i32, i32, i32, i32, V, V, V, V, V]
     L.nv_prepare_decode.restype = ctypes.c_int
     L.nv_prepare_prefill.argtypes = [V, V, V, i32, i32, i32, i32, i32, V, V, V, V, V, V, V]
@@ -126,6 +132,26 @@ def nv_store_kvcache(k, v, slot_mapping, k_cache, v_cache, d_err=None, stream=No
     rc = load_library().nv_store_kvcache(_ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(slot_mapping), n,
                                          _ptr(k_cache), _ptr(v_cache), nb * bs, hkv, d, _ptr(d_err), _stream(stream))
     _check("nv_store_kvcache", rc)
+
+
+def nv_sample_exponential_race(logits, temperatures, draws, tokens=None, workspace=None, d_err=None, stream=None):
+    """Token per row: argmax_i softmax(logits / T)_i / max(E_i, 1e-10) with ``draws`` E (int64 ``[B]``)."""
+    import torch
+    _need(logits.dim() == 2 and logits.stride(1) == 1 and draws.dim() == 2 and draws.stride(1) == 1,
+          "logits and draws must be [B, V] with unit column stride")
+    B, V = (int(x) for x in logits.shape)
+    _need(tuple(draws.shape) == (B, V) and int(temperatures.shape[0]) == B, "one temperature and V draws per row")
+    if tokens is None:
+        tokens = torch.empty(B, dtype=torch.int64, device=logits.device)
+    if workspace is None:
+        workspace = torch.empty(max(int(load_library().nv_sample_workspace_size(B, V)), 16), dtype=torch.uint8,
+                                device=logits.device)
+    rc = load_library().nv_sample_exponential_race(_ptr(logits), logits.stride(0), _ptr(temperatures), _ptr(draws),
+                                                   draws.stride(0), B, V, _ptr(tokens), _ptr(workspace),
+                                                   workspace.numel() * workspace.element_size(), _ptr(d_err),
+                                                   _stream(stream))
+    _check("nv_sample_exponential_race", rc)
+    return tokens
 
 
 def nv_prepare_decode(seq_lens, block_tables, block_size, num_blocks, padded_seqs=None, out=None, d_err=None,

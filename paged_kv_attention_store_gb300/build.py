@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(OUT_DIR, "libnv_paged_kv.so")
-SOURCES = ["abi_common.cu", "store_kvcache.cu", "paged_decode.cu", "paged_prefill.cu", "qk_norm_rope.cu", "prepare_meta.cu"]
+SOURCES = ["abi_common.cu", "store_kvcache.cu", "paged_decode.cu", "paged_prefill.cu", "qk_norm_rope.cu", "prepare_meta.cu", "sampler.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
           "--expt-relaxed-constexpr"]

@@ -133,6 +133,22 @@ def test_prepare_validation(lib):
                                   None) == NV_ERR_UNSUPPORTED
 
 
+def test_sampler_validation(lib):
+    assert lib.nv_sample_workspace_size(512, 151936) > 0
+    args = dict(lg=FAKE, ls=1024, t=FAKE, e=FAKE, es=1024, B=4, V=1000, tok=FAKE, ws=FAKE, wsb=1 << 20)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return lib.nv_sample_exponential_race(a["lg"], a["ls"], a["t"], a["e"], a["es"], a["B"], a["V"], a["tok"],
+                                              a["ws"], a["wsb"], None, None)
+    assert call(B=0, lg=None) == 0
+    assert call(lg=None) == NV_ERR_NULL
+    assert call(ls=999) == NV_ERR_SHAPE                    # stride shorter than the vocabulary
+    assert call(ls=1004) == NV_ERR_ALIGN                   # not a multiple of 8 entries
+    assert call(e=MISALIGNED) == NV_ERR_ALIGN
+    assert call(ws=None) == NV_ERR_WORKSPACE
+
+
 def _prefill(lib, q=FAKE, kc=FAKE, vc=FAKE, cq=FAKE, ck=FAKE, bt=FAKE, bts=8, B=2, tq=100, mq=80, hq=16, hkv=8,
              d=128, bs=256, nb=16, out=FAKE, ws=FAKE, wsb=256):
     return lib.nv_paged_prefill_attn(q, kc, vc, cq, ck, bt, bts, B, tq, mq, hq, hkv, d, bs, nb, 0.088, out, ws, wsb,
