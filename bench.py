@@ -667,6 +667,19 @@ def run_profile_case(case: str):
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
         return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
+    if case == "sampler-256rows":
+        # 256 rows x the 151936-entry vocabulary: 233 MB of logits + draws, above the L2
+        rng = np.random.default_rng([0, 17])
+        lg = to_dev(W.f32_to_bf16_bits((rng.standard_normal((256, 151936)) * 3.0).astype(np.float32)))
+        tm = torch.from_numpy(rng.uniform(0.5, 1.5, 256).astype(np.float32)).cuda()
+        dr = torch.from_numpy(rng.exponential(1.0, (256, 151936)).astype(np.float32)).cuda()
+        d_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for _ in range(3):
+            nv.nv_sample_exponential_race(lg, tm, dr, d_err=d_err)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_case": case, "d_err": int(d_err.item()),
+                          "algorithmic_bytes": 256 * 151936 * 6 + 256 * 12}))
+        return
     if case == "decode-64seq":
         ctx = np.random.default_rng([0, 200]).integers(1024, 4097, size=512)[:64]
         b = W.make_decode("qwen3-8b-decode-64", 0, ctx, 32, 8, 128, 256)
@@ -678,6 +691,18 @@ def run_profile_case(case: str):
     bt, lens = to_dev(b.block_tables), to_dev(b.seq_lens)
     cu_q, cu_k = to_dev(b.cu_seqlens_q), to_dev(b.cu_seqlens_k)
     d_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if case == "prologue-chunk":
+        pi = W.prologue_inputs(b, 0)
+        qkv, pos = to_dev(pi.qkv), to_dev(pi.positions)
+        qw, kw = to_dev(pi.q_weight), to_dev(pi.k_weight)
+        for _ in range(3):
+            nv.nv_qk_norm_rope_store(qkv, pos, qw, kw, slots, k_cache, v_cache, b.num_q_heads, rms_eps=pi.eps,
+                                     rope_theta=pi.theta, d_err=d_err)
+        torch.cuda.synchronize()
+        n = int(b.q_lens.sum())
+        print(json.dumps({"profile_case": case, "d_err": int(d_err.item()),
+                          "algorithmic_bytes": n * (b.num_q_heads + 2 * b.num_kv_heads) * 128 * 4 + n * 8}))
+        return
     for _ in range(3):
         nv.nv_store_kvcache(k_new, v_new, slots, k_cache, v_cache, d_err=d_err)
         if b.kind == "decode":
@@ -701,7 +726,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work per oracle baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seqs-per-step", type=int, default=1)
-    ap.add_argument("--profile-case", choices=["decode-64seq", "prefill-chunk"],
+    ap.add_argument("--profile-case", choices=["decode-64seq", "prefill-chunk", "prologue-chunk", "sampler-256rows"],
                     help="run one small case three times for an ncu capture and exit")
     args = ap.parse_args()
     if args.profile_case:
