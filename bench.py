@@ -111,6 +111,52 @@ def reduce_over_ranks(x: float, op: str, world: int, device="cpu") -> float:
     return float(t.item())
 
 
+def measure_decode_config(batch: W.PagedBatch, steps: int, warmup: int, dev) -> dict:
+    """Store + decode on another decode configuration; CUDA events around the decode call only."""
+    import torch
+
+    import paged_kv_attention_store_gb300 as nv
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    kc, vc = batch.cache()
+    k_cache, v_cache = to_dev(kc), to_dev(vc)
+    del kc, vc
+    q, k_new, v_new, slots = to_dev(batch.q), to_dev(batch.k_new), to_dev(batch.v_new), to_dev(batch.slot_mapping)
+    bt, lens = to_dev(batch.block_tables), to_dev(batch.seq_lens)
+    out = torch.empty_like(q)
+    maxc = int(batch.seq_lens.max())
+    ws = torch.empty(max(nv.nv_paged_decode_workspace_size(batch.num_seqs, batch.num_q_heads, 128, maxc), 16),
+                     dtype=torch.uint8, device=dev)
+    d_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(warmup + steps):
+        nv.nv_store_kvcache(k_new, v_new, slots, k_cache, v_cache, d_err=d_err)
+        if i >= warmup:
+            evs[i - warmup][0].record(stream)
+        nv.nv_paged_decode_attn(q, k_cache, v_cache, bt, lens, batch.scale, out=out, max_context_len=maxc,
+                                workspace=ws, d_err=d_err)
+        if i >= warmup:
+            evs[i - warmup][1].record(stream)
+    torch.cuda.synchronize()
+    assert int(d_err.item()) == 0, f"device error flags {int(d_err.item())}"
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    logical = decode_kv_bytes(batch)
+    used = batch.used_blocks([i for i in range(batch.num_seqs) if batch.seq_lens[i] > 0])
+    unique = len(used) * batch.block_size * batch.num_kv_heads * KV_BYTES_PER_TOKEN_PER_KVHEAD
+    del k_cache, v_cache
+    torch.cuda.empty_cache()
+    return {"ms_per_decode": round(ms, 4),
+            "attended_tok_s": round(float(batch.seq_lens.astype(np.int64).sum()) / (ms * 1e-3), 1),
+            "logical_kv_gbs": round(logical / (ms * 1e-3) / 1e9, 1),
+            "unique_kv_gbs": round(unique / (ms * 1e-3) / 1e9, 1),
+            "logical_kv_bytes": logical, "unique_kv_bytes": unique}
+
+
 def rank_decode_batch(rank: int, num_seqs: int = 512) -> W.PagedBatch:
     """Each rank's own Qwen3-8B-shaped decode batch (weak scaling: same shape, different seed)."""
     return W.qwen8_decode(seed=rank, num_seqs=num_seqs)
@@ -425,7 +471,14 @@ def run_ours(args, rank, world, local_rank):
         barrier()
         pro_ms = statistics.mean(a.elapsed_time(b) for a, b in rev)
         assert int(d_err.item()) == 0, f"device error flags {int(d_err.item())}"
-        assert int(d_err.item()) == 0, f"device error flags {int(d_err.item())}"
+
+        # the other decode configurations: Qwen3-0.6B decode with graph padding, long shared prefix
+        del pk_cache, pv_cache, flush
+        torch.cuda.empty_cache()
+        extra_steps = max(5, min(args.steps, 50))
+        cfg_q06 = measure_decode_config(W.qwen06_decode(seed=rank), extra_steps, args.warmup, dev)
+        cfg_sp = {bs: measure_decode_config(W.shared_prefix(seed=rank, block_size=bs), extra_steps, args.warmup, dev)
+                  for bs in (256, 16)}
     finally:
         sampler.__exit__(None, None, None)
 
@@ -544,6 +597,17 @@ def run_ours(args, rank, world, local_rank):
             "store": {"ms": round(store_ms_max, 4), "gbs": round(store_bytes / (store_ms_max * 1e-3) / 1e9, 1),
                       "bytes_per_step": store_bytes},
             "cpu_baseline": cpu_pf,
+        },
+        "qwen06_decode": {
+            "workload": "Qwen3-0.6B decode step: 256 seqs, ctx U[100, 2048], 16 q / 8 kv heads, bs 256, plus 32 "
+                        "graph-padding rows (slot -1, context 0); store 288 rows + decode",
+            **cfg_q06, "hbm_frac_of_peak": round(cfg_q06["logical_kv_gbs"] / hbm_peak, 4),
+        },
+        "shared_prefix": {
+            "workload": "64 seqs at context 4096, 32 q / 8 kv heads, the first 3072 tokens in the same physical "
+                        "blocks; logical KV 1.07 GB, unique 281 MB",
+            "bs256": cfg_sp[256], "bs16": cfg_sp[16],
+            "bs16_slowdown": round(cfg_sp[16]["ms_per_decode"] / cfg_sp[256]["ms_per_decode"], 3),
         },
         "prologue": {
             "kernel": "qk_norm_rope_store_kernel (nv_qk_norm_rope_store)",
@@ -683,6 +747,8 @@ def run_profile_case(case: str):
     if case == "decode-64seq":
         ctx = np.random.default_rng([0, 200]).integers(1024, 4097, size=512)[:64]
         b = W.make_decode("qwen3-8b-decode-64", 0, ctx, 32, 8, 128, 256)
+    elif case.startswith("shared-prefix-bs"):
+        b = W.shared_prefix(block_size=int(case[len("shared-prefix-bs"):]))
     else:
         b = W.prefill_chunk()
     kc, vc = b.cache()
@@ -726,7 +792,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work per oracle baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seqs-per-step", type=int, default=1)
-    ap.add_argument("--profile-case", choices=["decode-64seq", "prefill-chunk", "prologue-chunk", "sampler-256rows"],
+    ap.add_argument("--profile-case", choices=["decode-64seq", "prefill-chunk", "prologue-chunk", "sampler-256rows",
+                                               "shared-prefix-bs256", "shared-prefix-bs16"],
                     help="run one small case three times for an ncu capture and exit")
     args = ap.parse_args()
     if args.profile_case:
