@@ -276,10 +276,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const Pla
     for (int i = tid; i < kPlanBuckets; i += kPlanThreads)
         hist[i] = 0;
     __syncthreads();
-    for (int b = tid; b < pp.num_seqs; b += kPlanThreads) {
+    // a warp per sequence, its lanes over the sequence's tiles
+    for (int b = warp; b < pp.num_seqs; b += kPlanThreads / 32) {
         int cq0, Lq, P, T;
         if (plan_seq(pp, b, cq0, Lq, P, T))
-            for (int t = 0; t < T; ++t)
+            for (int t = lane; t < T; t += 32)
                 atomicAdd(&hist[min(tile_steps(P, Lq, t * pp.tq, pp.tq), kPlanBuckets - 1)], 1);
     }
     __syncthreads();
@@ -323,11 +324,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const Pla
     }
     __syncthreads();
     int4 *rec = reinterpret_cast<int4 *>(pp.ws + kPlanHeaderInts);
-    for (int b = tid; b < pp.num_seqs; b += kPlanThreads) {
+    for (int b = warp; b < pp.num_seqs; b += kPlanThreads / 32) {
         int cq0, Lq, P, T;
         if (!plan_seq(pp, b, cq0, Lq, P, T))
             continue;
-        for (int t = 0; t < T; ++t) {
+        for (int t = lane; t < T; t += 32) {
             const int i0 = t * pp.tq;
             const int nkv = tile_steps(P, Lq, i0, pp.tq);
             const int e = atomicAdd(&hist[min(nkv, kPlanBuckets - 1)], 1);
@@ -358,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int total = p.ws[1] * p.num_kv_heads;      // claims: work-list entries x kv heads
+    int total = 0;                                   // claims: work-list entries x kv heads (below)
 
     const uint32_t bar = base + kOffBar;
     auto BAR = [&](int i) { return bar + 8u * (uint32_t)i; };
@@ -419,6 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The work list comes from the pre-pass launched just before; this kernel is its programmatic
+    // dependent, so the setup above overlapped it.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    total = p.ws[1] * p.num_kv_heads;
     if (warp < 4) {
         warpgroup_reg_alloc<kSoftmaxRegs>();
         // ======================= softmax / correction (warps 0-3) =======================
@@ -1062,6 +1067,19 @@ extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const v
     // entries heaviest first
     const int64_t claims = cap * num_kv_heads;
     const int grid = (int)(claims < sms ? claims : sms);
-    paged_prefill_kernel<<<grid, kThreads, kSmemBytes, (cudaStream_t)stream>>>(tq_map, tk, tv, to, p);
+    // launched as a programmatic dependent of the pre-pass: its CTAs set up (barriers, TMEM, tensor
+    // maps) while the pre-pass runs, and wait for the work list with griddepcontrol.wait
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, paged_prefill_kernel, tq_map, tk, tv, to, p) != cudaSuccess)
+        return NV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
