@@ -13,13 +13,13 @@
 // the next tile's first scores are computed while the current tile finishes.
 //   * a one-CTA pre-pass lists the non-empty query tiles, heaviest first (counting sort by
 //     128-key steps), in the caller's workspace; a claim is one atomic add on a counter there.
-//   * warp 4 (TMA producer): claims tiles and passes them to the other warps through a small
-//     queue in shared memory.  Copies go out in the order they are needed: a tile's Q (one 3-D
-//     tensor-map copy per 64-dim half; dims head_dim, q head, token) into one of two Q buffers,
-//     K and V tiles of 128 keys x 128 dims straight from the paged pool (dims head_dim, kv
-//     head, slot), 128-byte swizzled, into a 3-slot K ring and a 2-slot V ring, K running two
-//     steps ahead of V as the MMAs consume them.  Lane i copies box i of a step; the block-table
-//     row is held 32 entries at a time in the warp's registers.
+//   * warps 4 and 11 (TMA producers): warp 4 claims tiles and passes them to the other warps
+//     through a small queue in shared memory, and copies each tile's Q (one 3-D tensor-map copy
+//     per 64-dim half; dims head_dim, q head, token) into one of two Q buffers and its K tiles
+//     (128 keys x 128 dims straight from the paged pool: dims head_dim, kv head, slot; 128-byte
+//     swizzled) into a 3-slot K ring; warp 11 copies the V tiles into a 2-slot V ring, each as
+//     soon as its slot is free, so a late K slot never holds up a V copy.  Lane i copies box i of
+//     a step; the block-table row is held 32 entries at a time in the warp's registers.
 //   * warps 5 and 6 (MMA issuers; warp 5 owns the TMEM allocation): one lane of warp 5 issues
 //     S(n) = Q K(n)^T (operands in shared memory), one lane of warp 6 issues O += P(n) V(n)
 //     (P read from tensor memory), tcgen05.mma kind::f16 with fp32 accumulators.  TMEM holds
@@ -59,11 +59,11 @@ constexpr int kQBufs = 2;            // Q buffers: the next item's Q loads while
 constexpr int kKSlots = NVKV_PREFILL_KSLOTS;   // K ring slots
 constexpr int kVSlots = 5 - kKSlots;           // V ring slots
 constexpr int kBufs = 3;             // score / P buffers in TMEM
-// Warp roles: 0-3 softmax (warpgroup 0); 4 TMA producer; 5 S = Q K^T issuer (owns TMEM); 6 O += P V
-// issuer; 7-10 epilogue (TMEM lane quarter = warp % 4); 11 idle.  Warpgroup 0 runs with more
+// Warp roles: 0-3 softmax (warpgroup 0); 4 TMA producer of Q and K; 5 S = Q K^T issuer (owns TMEM);
+// 6 O += P V issuer; 7-10 epilogue (TMEM lane quarter = warp % 4); 11 TMA producer of V.  Warpgroup 0 runs with more
 // registers than the others (setmaxnreg); the split must add up to the launch budget.
 constexpr int kThreads = 384;
-constexpr int kWarpProducer = 4, kWarpS = 5, kWarpPV = 6, kWarpEpi0 = 7, kWarpEpiEnd = 11;
+constexpr int kWarpProducer = 4, kWarpS = 5, kWarpPV = 6, kWarpEpi0 = 7, kWarpEpiEnd = 11, kWarpVProducer = 11;
 constexpr int kLaunchRegs = 168;                       // per thread at launch (checked on the host)
 constexpr int kSoftmaxRegs = 200, kOtherRegs = 152;
 static_assert(4 * kSoftmaxRegs + 8 * kOtherRegs == 12 * kLaunchRegs, "register split must match the launch");
@@ -96,7 +96,7 @@ constexpr int kBarOFree = kBarODone + kBufs;       // + item parity: the epilogu
 constexpr int kBarRowSum = kBarOFree + 2;          // + item parity: the softmax has written the row sums
 constexpr int kBarItemFull = kBarRowSum + 2;       // + queue slot
 constexpr int kBarItemEmpty = kBarItemFull + kQueue;
-constexpr int kItemReaders = 2 + 4 + 4;            // S cursor, PV cursor, 4 softmax, 4 epilogue warps
+constexpr int kItemReaders = 2 + 4 + 4 + 1;        // S cursor, PV cursor, 4 softmax, 4 epilogue warps, V copies
 constexpr int kNumBars = kBarItemEmpty + kQueue;
 constexpr uint32_t kOffItems = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffRowSum = kOffItems + kQueue * kItemInts * 4;   // float [2 item parities][128 rows]
@@ -224,8 +224,12 @@ struct Item {
 
 // ---------------------------------------------------------------------------------------
 // Work list.  A one-CTA pre-pass lists every non-empty query tile of every sequence (all kv
-// heads share an entry) in the workspace, ordered by its number of 128-key steps, heaviest
-// first (a counting sort), validates the lengths, and zeroes the claim counter.  The main
+// heads share an entry) in the workspace, validates the lengths, and zeroes the claim counter.
+// The list runs sequence by sequence, heaviest sequence first (a counting sort on the key steps
+// of its last tile), and within a sequence from its last (heaviest) tile to its first.  So the
+// CTAs busy at any moment work on one or two sequences, whose K/V then stays in L2 while every
+// tile of the sequence reads it (ordering all tiles by weight alone instead streamed the whole
+// batch's K/V from HBM once per wave), and the lightest tiles still come last.  The main
 // kernel's claim number v then names entry v / Hkv and kv head v % Hkv: a claim is one atomic
 // add and one 32-byte record load, with no empty tiles to skip.
 //   workspace ints: [0] claim counter, [1] entries, [16 + 8e ...] entry e:
@@ -267,6 +271,12 @@ __device__ __forceinline__ int tile_steps(int P, int Lq, int i0, int tq)
     return (P + i0 + min(tq, Lq - i0) + kBN - 1) / kBN;
 }
 
+// A sequence's sort bucket: the key steps of its last listed tile (its heaviest).
+__device__ __forceinline__ int seq_bucket(int P, int Lq, int T, int tq)
+{
+    return min(tile_steps(P, Lq, (T - 1) * tq, tq), kPlanBuckets - 1);
+}
+
 __global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const PlanParams pp)
 {
     __shared__ int hist[kPlanBuckets];
@@ -276,12 +286,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const Pla
     for (int i = tid; i < kPlanBuckets; i += kPlanThreads)
         hist[i] = 0;
     __syncthreads();
-    // a warp per sequence, its lanes over the sequence's tiles
-    for (int b = warp; b < pp.num_seqs; b += kPlanThreads / 32) {
+    // a thread per sequence: its tiles go to the bucket of its heaviest (last) tile's steps
+    for (int b = tid; b < pp.num_seqs; b += kPlanThreads) {
         int cq0, Lq, P, T;
-        if (plan_seq(pp, b, cq0, Lq, P, T))
-            for (int t = lane; t < T; t += 32)
-                atomicAdd(&hist[min(tile_steps(P, Lq, t * pp.tq, pp.tq), kPlanBuckets - 1)], 1);
+        if (plan_seq(pp, b, cq0, Lq, P, T) && T > 0)
+            atomicAdd(&hist[seq_bucket(P, Lq, T, pp.tq)], T);
     }
     __syncthreads();
     // exclusive prefix sum with the buckets in DESCENDING order: thread tid owns 8 of them
@@ -324,14 +333,20 @@ __global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const Pla
     }
     __syncthreads();
     int4 *rec = reinterpret_cast<int4 *>(pp.ws + kPlanHeaderInts);
+    // a warp per sequence: it takes a run of entries in its bucket and lists its tiles there, last
+    // (heaviest) tile first
     for (int b = warp; b < pp.num_seqs; b += kPlanThreads / 32) {
         int cq0, Lq, P, T;
-        if (!plan_seq(pp, b, cq0, Lq, P, T))
+        if (!plan_seq(pp, b, cq0, Lq, P, T) || T == 0)
             continue;
+        int first = 0;
+        if (lane == 0)
+            first = atomicAdd(&hist[seq_bucket(P, Lq, T, pp.tq)], T);
+        first = __shfl_sync(0xffffffffu, first, 0);
         for (int t = lane; t < T; t += 32) {
             const int i0 = t * pp.tq;
             const int nkv = tile_steps(P, Lq, i0, pp.tq);
-            const int e = atomicAdd(&hist[min(nkv, kPlanBuckets - 1)], 1);
+            const int e = first + (T - 1 - t);
             if (e < pp.cap) {
                 const int nq = min(pp.tq, Lq - i0);
                 rec[2 * e] = make_int4(b, cq0, Lq, P);
@@ -523,52 +538,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             flag_error(p.d_err, NV_DERR_TIMEOUT);
     } else {
         warpgroup_reg_dealloc<kOtherRegs>();
+        // this lane's box of key tile n of an item (its first pool slot, -1 = none); the block-table
+        // row is held 32 entries at a time in the warp's registers (win, from entry win_base)
+        const int bs_mask = (1 << p.block_shift) - 1;
+        const int boxes = kBN / p.box_rows;
+        auto box_slot = [&](const Item &it, int n, const int32_t *bt, int nblk, int &win_base, int &win) {
+            const int lb0 = (n * kBN) >> p.block_shift;
+            const int lb_hi = min(lb0 + boxes - 1, nblk - 1);
+            if (lb_hi >= win_base + 32) {               // warp-uniform window move
+                win_base = lb0;
+                win = win_base + lane < nblk ? __ldg(bt + win_base + lane) : -1;
+            }
+            const int j0 = n * kBN + lane * p.box_rows;
+            const int lb = j0 >> p.block_shift;
+            const int blk = __shfl_sync(0xffffffffu, win, (lb - win_base) & 31);
+            int slot = -1;
+            if (lane < boxes && j0 < it.kv_len) {
+                if (blk < 0 || blk >= p.num_blocks)
+                    flag_error(p.d_err, NV_DERR_BLOCK_RANGE);
+                else
+                    slot = (blk << p.block_shift) + (j0 & bs_mask);
+            }
+            return slot;
+        };
+        // copy one K or V tile (global key tile idx) into its ring; the slot's previous tile
+        // (idx - slots) is free once its MMA group has completed: S for K, PV for V, whose commits
+        // to the score-buffer barriers already signal that.  Lane kb copies box kb (box_rows keys,
+        // both 64-dim halves).
+        auto copy_tile = [&](bool is_v, int idx, int kvh, int slot) {
+            const int n_slots = is_v ? kVSlots : kKSlots;
+            const int s_ = idx % n_slots;
+            const uint32_t full = BAR((is_v ? kBarVFull : kBarKFull) + s_);
+            const int prev = idx - n_slots;
+            if (prev >= 0 &&
+                !__all_sync(0xffffffffu,
+                            mbar_wait(BAR((is_v ? kBarODone : kBarSFull) + prev % kBufs), (prev / kBufs) & 1)))
+                return false;
+            const uint32_t bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, slot >= 0)) * p.box_rows * 256u;
+            const uint32_t dst = base + (is_v ? kOffV : kOffK) + s_ * kTile + (uint32_t)lane * p.box_rows * 128u;
+            if (lane == 0)
+                mbar_arrive_expect_tx(full, bytes);
+            __syncwarp();
+            if (slot >= 0) {
+                const CUtensorMap *map = is_v ? &tmap_v : &tmap_k;
+                tma_load_3d(dst, map, 0, kvh, slot, full);
+                tma_load_3d(dst + kHalf, map, 64, kvh, slot, full);
+            }
+            return true;
+        };
         if (warp == kWarpProducer) {
-            // =========================== TMA producer ===========================
-            // Copies go out in the order the MMA issuer needs them.  S(j) is issued two key tiles
-            // before PV(j), so K(j) is copied two tiles ahead of V(j): the stream is K(j) V(j-2),
-            // K(j+1) V(j-1), ...  An item's Q tile goes out just before its first K tile (after the
-            // V copy that precedes it: that V feeds the PV whose completion frees the Q buffer).
-            // Lane kb copies box kb of a tile (box_rows keys, both 64-dim halves).
-            const int bs_mask = (1 << p.block_shift) - 1;
-            const int boxes = kBN / p.box_rows;
+            // ====================== TMA producer: work items, Q and K ======================
+            // Claims items and queues them; copies each item's Q tile (one 3-D tensor-map copy
+            // per 64-dim half) into one of two Q buffers just before the item's first K tile, and
+            // its K tiles into the K ring as the S issuer frees the slots.
             if (lane == 0) {
                 prefetch_tmap(&tmap_q);
                 prefetch_tmap(&tmap_k);
-                prefetch_tmap(&tmap_v);
                 prefetch_tmap(&tmap_o);
             }
-            struct TileCopy {
-                int slot;           // this lane's box: first pool slot, -1 = none
-                int kvh;
-                uint32_t bytes;     // whole tile
-            };
-            // copy one K or V tile into its ring (idx = its global key tile).  The slot's previous
-            // tile (idx - slots) is free once its MMA group has completed: S for K, PV for V, whose
-            // commits to the score-buffer barriers already signal that.
-            auto copy_tile = [&](bool is_v, int idx, const TileCopy &c) {
-                const int n_slots = is_v ? kVSlots : kKSlots;
-                const int s_ = idx % n_slots;
-                const uint32_t full = BAR((is_v ? kBarVFull : kBarKFull) + s_);
-                const int prev = idx - n_slots;
-                if (prev >= 0 &&
-                    !__all_sync(0xffffffffu,
-                                mbar_wait(BAR((is_v ? kBarODone : kBarSFull) + prev % kBufs), (prev / kBufs) & 1)))
-                    return false;
-                const uint32_t dst = base + (is_v ? kOffV : kOffK) + s_ * kTile + (uint32_t)lane * p.box_rows * 128u;
-                if (lane == 0)
-                    mbar_arrive_expect_tx(full, c.bytes);
-                __syncwarp();
-                if (c.slot >= 0) {
-                    const CUtensorMap *map = is_v ? &tmap_v : &tmap_k;
-                    tma_load_3d(dst, map, 0, c.kvh, c.slot, full);
-                    tma_load_3d(dst + kHalf, map, 64, c.kvh, c.slot, full);
-                }
-                return true;
-            };
             bool ok = true;
             int j = 0;                                  // global key tile of the next K copy
-            TileCopy v1{-1, 0, 0}, v2{-1, 0, 0};        // tiles j-1 and j-2, whose V is still to copy
             // lane 0 claims one item ahead: the counter's answer for item k+1 travels while item k's
             // copies are issued
             const int4 *plan = reinterpret_cast<const int4 *>(p.ws + kPlanHeaderInts);
@@ -622,32 +651,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 const int32_t *bt = p.block_tables + (size_t)it.b * p.bt_stride;
                 const int nblk = (it.kv_len + (1 << p.block_shift) - 1) >> p.block_shift;
-                int win_base = 0;                       // the block-table row, 32 entries at a time
+                int win_base = 0;
                 int win = lane < nblk ? __ldg(bt + lane) : -1;
-                for (int n = 0; n < it.nkv && ok; ++n) {
-                    // this lane's box of tile n
-                    TileCopy cur{-1, it.kvh, 0};
-                    const int lb0 = (n * kBN) >> p.block_shift;
-                    const int lb_hi = min(lb0 + boxes - 1, nblk - 1);
-                    if (lb_hi >= win_base + 32) {       // warp-uniform window move
-                        win_base = lb0;
-                        win = win_base + lane < nblk ? __ldg(bt + win_base + lane) : -1;
-                    }
-                    const int j0 = n * kBN + lane * p.box_rows;
-                    const int lb = j0 >> p.block_shift;
-                    const int blk = __shfl_sync(0xffffffffu, win, (lb - win_base) & 31);
-                    if (lane < boxes && j0 < it.kv_len) {
-                        if (blk < 0 || blk >= p.num_blocks)
-                            flag_error(p.d_err, NV_DERR_BLOCK_RANGE);
-                        else
-                            cur.slot = (blk << p.block_shift) + (j0 & bs_mask);
-                    }
-                    cur.bytes = (uint32_t)__popc(__ballot_sync(0xffffffffu, cur.slot >= 0)) * p.box_rows * 256u;
+                for (int n = 0; n < it.nkv && ok; ++n, ++j) {
+                    const int slot = box_slot(it, n, bt, nblk, win_base, win);
                     if (n == 0) {
-                        if (j >= 2 && !copy_tile(true, j - 2, v2)) {
-                            ok = false;
-                            break;
-                        }
                         // the item's Q, into buffer k % 2 once item k-2's last S and epilogue are done
                         const int qb = k % kQBufs;
                         if (k >= kQBufs &&
@@ -661,26 +669,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tma_load_3d(base + kOffQ + qb * kTile + h * kHalf, &tmap_q, h * 64,
                                             it.kvh * p.group, it.cq0 + it.i0, BAR(kBarQFull + qb));
                         }
-                        if (!copy_tile(false, j, cur)) {
-                            ok = false;
-                            break;
-                        }
-                    } else {
-                        if (!copy_tile(false, j, cur) || (j >= 2 && !copy_tile(true, j - 2, v2))) {
-                            ok = false;
-                            break;
-                        }
                     }
-                    v2 = v1;
-                    v1 = cur;
-                    ++j;
+                    ok = copy_tile(false, j, it.kvh, slot);
                 }
             }
-            // the last two V tiles
-            if (ok && j >= 2)
-                ok = copy_tile(true, j - 2, v2);
-            if (ok && j >= 1)
-                ok = copy_tile(true, j - 1, v1);
+            if (!ok && lane == 0)
+                flag_error(p.d_err, NV_DERR_TIMEOUT);
+        } else if (warp == kWarpVProducer) {
+            // ========================= TMA producer: V =========================
+            // Copies each item's V tiles into the V ring as soon as the PV issuer frees a slot,
+            // independently of the K stream.
+            if (lane == 0)
+                prefetch_tmap(&tmap_v);
+            bool ok = true;
+            int j = 0;                                  // global key tile of the next V copy
+            Item it;
+            for (int k = 0; ok; ++k) {
+                if (!read_item(k, it)) {
+                    ok = false;
+                    break;
+                }
+                if (it.v >= total)
+                    break;
+                const int32_t *bt = p.block_tables + (size_t)it.b * p.bt_stride;
+                const int nblk = (it.kv_len + (1 << p.block_shift) - 1) >> p.block_shift;
+                int win_base = 0;
+                int win = lane < nblk ? __ldg(bt + lane) : -1;
+                for (int n = 0; n < it.nkv && ok; ++n, ++j)
+                    ok = copy_tile(true, j, it.kvh, box_slot(it, n, bt, nblk, win_base, win));
+            }
             if (!ok && lane == 0)
                 flag_error(p.d_err, NV_DERR_TIMEOUT);
         } else if (warp == kWarpS || warp == kWarpPV) {
