@@ -8,11 +8,12 @@
 // How (GB300 design; the pages call a library kernel here).  The unit of work is one 128-row
 // query tile of one (sequence, kv head); with G = Hq/Hkv query heads per kv head the tile packs
 // 128/G consecutive tokens x G heads, so every K/V tile loaded serves all G heads.  The kernel
-// is persistent (one CTA per SM): CTAs claim tiles, heaviest first, from a counter in the
+// is persistent (one CTA per SM): CTAs claim tiles in work-list order from a counter in the
 // caller's workspace, and each CTA runs its tiles as one continuous stream of 128-key steps, so
 // the next tile's first scores are computed while the current tile finishes.
-//   * a one-CTA pre-pass lists the non-empty query tiles, heaviest first (counting sort by
-//     128-key steps), in the caller's workspace; a claim is one atomic add on a counter there.
+//   * a one-CTA pre-pass lists the non-empty query tiles in the caller's workspace, sequence by
+//     sequence (heaviest sequence first, each sequence's tiles heaviest first), so the CTAs at
+//     work share a few sequences' K/V in L2; a claim is one atomic add on a counter there.
 //   * warps 4 and 11 (TMA producers): warp 4 claims tiles and passes them to the other warps
 //     through a small queue in shared memory, and copies each tile's Q (one 3-D tensor-map copy
 //     per 64-dim half; dims head_dim, q head, token) into one of two Q buffers and its K tiles
@@ -35,8 +36,8 @@
 //     a score beats it by more than 8; only then is O rescaled in TMEM), and writes P with
 //     tcgen05.st.  At a tile's end it normalises O, stages the bf16 rows in the tile's Q buffer
 //     (free once the last PV is done) and writes them with tensor-map stores.
-// Measured on GB300: an M=128 tcgen05.mma costs about the same for N=64 as for N=128 (so key
-// steps are 128 wide), and loading 128 fp32 scores from TMEM takes ~100 cycles.
+// Measured on GB300: an M=128 K=16 tcgen05.mma fed back to back takes 64 cycles at N=128 and 48
+// at N=64 (so key steps are 128 wide), and loading 128 fp32 scores from TMEM takes ~30 cycles.
 // Every mbarrier wait is bounded; on timeout the kernel records NV_DERR_TIMEOUT and stops.
 #include <cuda.h>
 
@@ -1081,7 +1082,7 @@ extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const v
         return NV_ERR_UNSUPPORTED;
     prefill_plan_kernel<<<1, kPlanThreads, 0, (cudaStream_t)stream>>>(pp);
     // persistent: one CTA per SM (shared memory and TMEM admit one); CTAs claim the work list's
-    // entries heaviest first
+    // entries in order
     const int64_t claims = cap * num_kv_heads;
     const int grid = (int)(claims < sms ? claims : sms);
     // launched as a programmatic dependent of the pre-pass: its CTAs set up (barriers, TMEM, tensor
