@@ -104,3 +104,23 @@ def test_prefill_grid_hint_smaller_than_chunk_is_flagged():
     db.store()
     db.prefill(max_seqlen_q=100)
     assert db.err() & nv.NV_DERR_LENGTH
+
+
+def test_prefill_many_sequences_and_long_chunk_sampled():
+    """1200 sequences (more than the pre-pass has threads, and many sharing one sort bucket) with
+    short chunks over assorted prefixes, plus one 2500-token chunk (more query tiles than a warp
+    has lanes): every listed tile must be computed once, whatever its place in the work list."""
+    rng = np.random.default_rng(7)
+    n = 1200
+    prefix = (rng.integers(0, 9, n) * 64).tolist() + [300]
+    chunk = rng.integers(1, 40, n).tolist() + [2500]
+    b = W.make_prefill("many", 41, prefix, chunk, 16, 8, 128, 64)
+    db, got, kc, vc = _run(b)
+    cu = b.cu_seqlens_q
+    rows = set(rng.choice(int(cu[-1]) - 2500, 160, replace=False).tolist())
+    lo = int(cu[-2])
+    rows |= {lo, lo + 63, lo + 64, lo + 2047, lo + 2048, lo + 2111, lo + 2112, lo + 2499}
+    rows |= set((lo + rng.choice(2500, 40, replace=False)).tolist())
+    rows = np.array(sorted(rows), np.int64)
+    want = oracle_prefill(oracle.default(), b, kc, vc, rows=rows, threads=16)
+    compare(got[rows], want, "prefill many sequences")
