@@ -14,6 +14,9 @@
 // their rotation partners 64+2l, 64+2l+1, so the rotation needs no shuffles and every load and
 // store is a coalesced 128-byte row half; the sum of squares is a 5-level butterfly.  The loads
 // of kItems heads go out together before any arithmetic, to keep enough bytes in flight for HBM.
+// The two bf16 roundings work on pairs: one conversion rounds two normalised values, and one
+// bf16x2 multiply forms both weight products (the kernel is issue-bound, so instruction count
+// matters).
 // The RoPE frequencies are computed once per call on the host (64 floats, passed as a kernel
 // parameter); the angle product and sincosf are fp32, as the pages compute them.
 #include <cmath>
@@ -52,9 +55,13 @@ __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t v)
     return make_float2(bf16lo(v), bf16hi(v));
 }
 
-__device__ __forceinline__ float round_bf16_f(float x)
+// bf16x2 product, rounded to nearest: the exact product of two bf16 values fits in fp32, so this
+// equals rounding the fp32 product to bf16 (the pages' bf16 multiply by the norm weight)
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
 {
-    return __bfloat162float(__float2bfloat16_rn(x));
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 __global__ void __launch_bounds__(kWarps * 32) qk_norm_rope_store_kernel(const __grid_constant__ RopeParams p)
@@ -66,10 +73,10 @@ __global__ void __launch_bounds__(kWarps * 32) qk_norm_rope_store_kernel(const _
     const int64_t warp_id = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * kWarps;
     // this lane's weights (dims 2l, 2l+1 and 64+2l, 64+2l+1) and frequencies (2l, 2l+1)
-    const float2 qw1 = bf16x2_to_f2(__ldg(reinterpret_cast<const uint32_t *>(p.q_weight) + lane));
-    const float2 qw2 = bf16x2_to_f2(__ldg(reinterpret_cast<const uint32_t *>(p.q_weight) + 32 + lane));
-    const float2 kw1 = bf16x2_to_f2(__ldg(reinterpret_cast<const uint32_t *>(p.k_weight) + lane));
-    const float2 kw2 = bf16x2_to_f2(__ldg(reinterpret_cast<const uint32_t *>(p.k_weight) + 32 + lane));
+    const uint32_t qw1 = __ldg(reinterpret_cast<const uint32_t *>(p.q_weight) + lane);
+    const uint32_t qw2 = __ldg(reinterpret_cast<const uint32_t *>(p.q_weight) + 32 + lane);
+    const uint32_t kw1 = __ldg(reinterpret_cast<const uint32_t *>(p.k_weight) + lane);
+    const uint32_t kw2 = __ldg(reinterpret_cast<const uint32_t *>(p.k_weight) + 32 + lane);
     const float f0 = p.inv_freq[2 * lane], f1 = p.inv_freq[2 * lane + 1];
 
     // one warp per token: the token's angles are shared by all its heads
@@ -117,12 +124,11 @@ __global__ void __launch_bounds__(kWarps * 32) qk_norm_rope_store_kernel(const _
                 for (int o = 16; o > 0; o >>= 1)
                     ss += __shfl_xor_sync(0xffffffffu, ss, o);
                 const float r = rsqrtf(ss * (1.0f / kD) + p.eps);
-                const float2 w1 = is_q ? qw1 : kw1, w2 = is_q ? qw2 : kw2;
-                // cast to bf16, then the bf16 product with the weight
-                const float n0 = round_bf16_f(round_bf16_f(x1.x * r) * w1.x);
-                const float n1 = round_bf16_f(round_bf16_f(x1.y * r) * w1.y);
-                const float n2 = round_bf16_f(round_bf16_f(x2.x * r) * w2.x);
-                const float n3 = round_bf16_f(round_bf16_f(x2.y * r) * w2.y);
+                const uint32_t w1 = is_q ? qw1 : kw1, w2 = is_q ? qw2 : kw2;
+                // cast to bf16 (two values per conversion), then the bf16 product with the weight
+                const float2 na = bf16x2_to_f2(mul_bf16x2(pack_bf16x2(x1.x * r, x1.y * r), w1));
+                const float2 nb = bf16x2_to_f2(mul_bf16x2(pack_bf16x2(x2.x * r, x2.y * r), w2));
+                const float n0 = na.x, n1 = na.y, n2 = nb.x, n3 = nb.y;
                 // RoPE, rotate-half: (n0, n2) at frequency 2l, (n1, n3) at frequency 2l+1
                 const uint32_t y1 = pack_bf16x2(n0 * c0 - n2 * s0, n1 * c1 - n3 * s1);
                 const uint32_t y2 = pack_bf16x2(n2 * c0 + n0 * s0, n3 * c1 + n1 * s1);
@@ -187,7 +193,7 @@ extern "C" int nv_qk_norm_rope_store(const void *qkv, int64_t qkv_row_stride, co
         p.inv_freq[j] = 1.0f / powf(rope_theta, (float)(2 * j) / (float)kD);
 
     const int64_t blocks_needed = ((int64_t)n_tokens + kWarps - 1) / kWarps;
-    const int64_t cap = (int64_t)sms * 8;
+    const int64_t cap = (int64_t)sms * 4;      // half the resident limit: measured a little faster
     const int grid = (int)(blocks_needed < cap ? blocks_needed : cap);
     qk_norm_rope_store_kernel<<<grid, kWarps * 32, 0, (cudaStream_t)stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
