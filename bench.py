@@ -300,6 +300,7 @@ def run_ours(args, rank, world, local_rank):
         dec_ms = t_start.elapsed_time(t_end)
         dec_kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
         assert int(d_err.item()) == 0, f"device error flags {int(d_err.item())}"
+        dec_out_bits = host_bits(out)             # checked against the oracle's sample below
 
         # e2e: the same step through the public API from pinned HOST buffers, inputs copied in
         # and the output read back every step
@@ -445,6 +446,7 @@ def run_ours(args, rank, world, local_rank):
             flush.fill_(i & 0xFF)          # L2 flush between steps, outside the step's events
             prefill_step(pev[i])
         barrier()
+        pf_out_bits = host_bits(pout)
         store_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in pev)
         pf_ms = statistics.mean(b.elapsed_time(c) for _, b, c in pev)
         pf_step_ms = statistics.mean(a.elapsed_time(c) for a, _, c in pev)
@@ -509,8 +511,22 @@ def run_ours(args, rank, world, local_rank):
 
     if rank != 0:
         return None
-    cpu = None if args.no_cpu_baseline else cpu_baseline_decode(db, args.cpu_seconds)
-    cpu_pf = None if args.no_cpu_baseline else cpu_baseline_prefill(pb, args.cpu_seconds)
+    dec_want, pf_want = {}, {}
+    cpu = None if args.no_cpu_baseline else cpu_baseline_decode(db, args.cpu_seconds, collect=dec_want)
+    cpu_pf = None if args.no_cpu_baseline else cpu_baseline_prefill(pb, args.cpu_seconds, collect=pf_want)
+    parity = None
+    if dec_want and pf_want:
+        ds = sorted(dec_want)
+        pr = np.array(sorted(pf_want), np.int64)
+        parity = {
+            "decode": dict(output_error(dec_out_bits[ds], np.stack([dec_want[i] for i in ds])),
+                           sample=f"{len(ds)} sequences x {db.num_q_heads} heads of the timed batch"),
+            "prefill": dict(output_error(pf_out_bits[pr], np.stack([pf_want[int(i)] for i in pr])),
+                            sample=f"{pr.size} query rows x {pb.num_q_heads} heads of the timed batch"),
+            "bar": {"max_abs": 2e-2, "mean_abs": 2e-3},
+            "note": "GPU outputs of the timed runs against the fp32 oracle's outputs for the rows its baseline "
+                    "leg computed",
+        }
     clocks = sampler.summary()
     hbm_peak = float(pk["hbm_gbs"])
     tc_peak = float(pk["bf16_tflops"])
@@ -546,6 +562,7 @@ def run_ours(args, rank, world, local_rank):
             "traffic": profiled_traffic("decode_qwen8", ["paged_decode.cu", "nv_common.cuh"]),
         },
         "cpu_baseline": cpu,
+        "parity": parity,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max / args.steps, 4)},
         "fused_store_decode": {
@@ -627,8 +644,24 @@ def run_ours(args, rank, world, local_rank):
 # CPU oracle (baseline leg and reference arm)
 # ----------------------------------------------------------------------------------------
 
-def cpu_baseline_decode(b: W.PagedBatch, seconds: float, max_seqs: int | None = None):
-    """Oracle decode, single thread, sequence by sequence until ~`seconds` of CPU work."""
+def host_bits(t) -> np.ndarray:
+    """bf16 tensor -> host uint16 bit patterns (a synchronous copy)."""
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def output_error(got_bits: np.ndarray, want: np.ndarray) -> dict:
+    """max-abs, mean-abs and relative L2 error of bf16 outputs against fp32 oracle outputs."""
+    got = W.bf16_bits_to_f32(got_bits).astype(np.float64)
+    want = np.asarray(want, np.float64)
+    err = np.abs(got - want)
+    return {"max_abs": float(err.max()), "mean_abs": float(err.mean()),
+            "rel_l2": float(np.linalg.norm(got - want) / max(float(np.linalg.norm(want)), 1e-30))}
+
+
+def cpu_baseline_decode(b: W.PagedBatch, seconds: float, max_seqs: int | None = None, collect: dict | None = None):
+    """Oracle decode, single thread, sequence by sequence until ~`seconds` of CPU work (outputs into
+    `collect`, by sequence, when given)."""
     import oracle
     orc = oracle.default()
     done, tokens, spent = 0, 0, 0.0
@@ -638,9 +671,11 @@ def cpu_baseline_decode(b: W.PagedBatch, seconds: float, max_seqs: int | None = 
         kc, vc = sub.cache(ids, threads=1)
         orc.store_kvcache(sub.k_new, sub.v_new, sub.slot_mapping, kc, vc)
         t0 = time.perf_counter()
-        orc.decode_attn(sub.q, kc, vc, sub.block_tables, sub.context_lens, sub.num_kv_heads, sub.block_size,
-                        sub.scale, threads=1)
+        o = orc.decode_attn(sub.q, kc, vc, sub.block_tables, sub.context_lens, sub.num_kv_heads, sub.block_size,
+                            sub.scale, threads=1)
         spent += time.perf_counter() - t0
+        if collect is not None:
+            collect[int(s)] = o[0]
         done += 1
         tokens += int(sub.seq_lens.sum())
         if spent >= seconds or (max_seqs and done >= max_seqs):
@@ -652,8 +687,9 @@ def cpu_baseline_decode(b: W.PagedBatch, seconds: float, max_seqs: int | None = 
             "seconds": round(spent, 2), "attended_tok_s": round(tokens / spent, 1)}
 
 
-def cpu_baseline_prefill(b: W.PagedBatch, seconds: float):
-    """Oracle prefill, single thread, on a random sample of query rows until ~`seconds`."""
+def cpu_baseline_prefill(b: W.PagedBatch, seconds: float, collect: dict | None = None):
+    """Oracle prefill, single thread, on a random sample of query rows until ~`seconds` (outputs into
+    `collect`, by row, when given)."""
     import oracle
     orc = oracle.default()
     kc, vc = b.cache(threads=1)
@@ -666,9 +702,12 @@ def cpu_baseline_prefill(b: W.PagedBatch, seconds: float):
         chunk = rows_all[i:i + 16]
         i += 16
         t0 = time.perf_counter()
-        orc.prefill_attn(b.q, kc, vc, b.cu_seqlens_q, b.cu_seqlens_k, b.block_tables, b.num_kv_heads,
-                         b.block_size, b.scale, rows=chunk, threads=1)
+        o = orc.prefill_attn(b.q, kc, vc, b.cu_seqlens_q, b.cu_seqlens_k, b.block_tables, b.num_kv_heads,
+                             b.block_size, b.scale, rows=chunk, threads=1)
         spent += time.perf_counter() - t0
+        if collect is not None:
+            for j, r in enumerate(chunk):
+                collect[int(r)] = o[j]
         for r in chunk:
             s = int(np.searchsorted(cu, r, side="right") - 1)
             pairs += int(P[s]) + int(r - cu[s]) + 1
