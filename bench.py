@@ -302,26 +302,36 @@ def run_ours(args, rank, world, local_rank):
         assert int(d_err.item()) == 0, f"device error flags {int(d_err.item())}"
         dec_out_bits = host_bits(out)             # checked against the oracle's sample below
 
-        # e2e: the same step through the public API from pinned HOST buffers, inputs copied in
-        # and the output read back every step
-        h_q = torch.from_numpy(db.q.view(np.int16)).view(torch.bfloat16).pin_memory()
-        h_k = torch.from_numpy(db.k_new.view(np.int16)).view(torch.bfloat16).pin_memory()
-        h_v = torch.from_numpy(db.v_new.view(np.int16)).view(torch.bfloat16).pin_memory()
-        h_s = torch.from_numpy(db.slot_mapping).pin_memory()
-        h_bt = torch.from_numpy(db.block_tables).pin_memory()
-        h_ctx = torch.from_numpy(db.seq_lens).pin_memory()
+        # e2e: the same step through the public API from pinned HOST memory: the step's inputs (q, the new
+        # K/V rows, slots, block tables, lengths) packed back to back in one staging buffer and copied in
+        # with one transfer, and the output read back, every step
+        host_parts = [db.q.view(np.uint8).ravel(), db.k_new.view(np.uint8).ravel(), db.v_new.view(np.uint8).ravel(),
+                      db.slot_mapping.view(np.uint8).ravel(), db.block_tables.view(np.uint8).ravel(),
+                      db.seq_lens.view(np.uint8).ravel()]
+        offs, total = [], 0
+        for a in host_parts:
+            offs.append(total)
+            total += (a.size + 255) // 256 * 256
+        h_stage = torch.zeros(total, dtype=torch.uint8).pin_memory()
+        hs = h_stage.numpy()
+        for o, a in zip(offs, host_parts):
+            hs[o:o + a.size] = a
+        d_stage = torch.empty(total, dtype=torch.uint8, device=dev)
+
+        def staged(k, like):
+            return d_stage[offs[k]:offs[k] + like.numel() * like.element_size()].view(like.dtype).view(like.shape)
+
+        q_e, k_e, v_e = staged(0, q), staged(1, k_new), staged(2, v_new)
+        s_e, bt_e, ctx_e = staged(3, slots), staged(4, bt), staged(5, ctx)
         h_out = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_s, h_bt, h_ctx))
+        h2d = total
         d2h = h_out.numel() * h_out.element_size()
 
         def e2e_step():
-            q.copy_(h_q, non_blocking=True)
-            k_new.copy_(h_k, non_blocking=True)
-            v_new.copy_(h_v, non_blocking=True)
-            slots.copy_(h_s, non_blocking=True)
-            bt.copy_(h_bt, non_blocking=True)
-            ctx.copy_(h_ctx, non_blocking=True)
-            decode_step()
+            d_stage.copy_(h_stage, non_blocking=True)
+            nv.nv_store_kvcache(k_e, v_e, s_e, k_cache, v_cache, d_err=d_err)
+            nv.nv_paged_decode_attn(q_e, k_cache, v_cache, bt_e, ctx_e, db.scale, out=out, max_context_len=maxc,
+                                    workspace=ws, d_err=d_err)
             h_out.copy_(out, non_blocking=True)
 
         for _ in range(args.warmup):
@@ -334,6 +344,9 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
         barrier()
         e2e_ms = e0.elapsed_time(e1)
+        torch.cuda.synchronize()
+        assert np.array_equal(h_out.view(torch.int16).numpy().view(np.uint16), dec_out_bits), \
+            "the staged end-to-end step must reproduce the device-resident step's output"
 
         # fused store + decode (one pass, nv_store_decode_attn) on the same batch
         def fused_step():
