@@ -129,7 +129,7 @@ def measure_decode_config(batch: W.PagedBatch, steps: int, warmup: int, dev) -> 
     bt, lens = to_dev(batch.block_tables), to_dev(batch.seq_lens)
     out = torch.empty_like(q)
     maxc = int(batch.seq_lens.max())
-    ws = torch.empty(max(nv.nv_paged_decode_workspace_size(batch.num_seqs, batch.num_q_heads, 128, maxc), 16),
+    ws = torch.zeros(max(nv.nv_paged_decode_workspace_size(batch.num_seqs, batch.num_q_heads, 128, maxc), 16),
                      dtype=torch.uint8, device=dev)
     d_err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
@@ -269,7 +269,7 @@ def run_ours(args, rank, world, local_rank):
     out = torch.empty_like(q)
     maxc = int(db.seq_lens.max())
     ws_bytes = nv.nv_paged_decode_workspace_size(db.num_seqs, db.num_q_heads, 128, maxc)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)      # split counters start at zero
     d_err = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def decode_step(ev=None):

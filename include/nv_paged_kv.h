@@ -203,8 +203,12 @@ size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
  *                 truncated to it and flagged NV_DERR_LENGTH.  <= bt_stride*block_size.
  *   scale         softmax scale (head_dim ** -0.5 in the pages).
  *   workspace     device scratch of at least nv_paged_decode_workspace_size(...) bytes
- *                 (may be NULL when that size is 0).  Calls that share a workspace must not
- *                 overlap on the device.
+ *                 (may be NULL when that size is 0), 16-byte aligned.  Its first 256 KiB hold
+ *                 the per-sequence split counters: they must be ZERO before the first call
+ *                 that uses the workspace (allocate it zero-filled), and every call leaves them
+ *                 zero, whatever the batch; the rest needs no initialisation.  Calls that share
+ *                 a workspace must not overlap on the device.  Batches of more than 65536
+ *                 sequences whose contexts need several splits return NV_ERR_UNSUPPORTED.
  */
 int nv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
                          const int32_t *block_tables, int32_t bt_stride, const int32_t *context_lens,
@@ -260,11 +264,12 @@ int nv_store_decode_attn(const void *q, const void *k, int64_t k_row_stride, con
  * array; a batch whose partials still exceed it (num_seqs * splits * num_q_heads * 520 bytes)
  * is rejected with NV_ERR_WORKSPACE before anything is enqueued.
  *
- * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ * The first call on a device looks up the arrays' device addresses (cudaGetSymbolAddress) with
  * that device current; make that first call before any stream capture.  All calls share the
- * one array and it keeps the last call's contents (nothing in it needs to start at zero):
- * calls that overlap on the GPU -- on different streams, or from different threads -- race on
- * it and give wrong results.  Serialise them.
+ * one scratch array (it keeps the last call's contents; nothing in it needs to start at zero)
+ * and one array of 65536 split counters (zero when the library loads; every call leaves them
+ * zero): calls that overlap on the GPU -- on different streams, or from different threads --
+ * race on them and give wrong results.  Serialise them.
  */
 #define NV_DECODE_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 

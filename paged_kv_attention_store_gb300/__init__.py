@@ -223,7 +223,9 @@ def nv_paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale,
 
     ``max_context_len`` (a host int bounding every context length) sizes the split-KV grid;
     by default it is the block table's capacity ``W * block_size``, which needs no device
-    read.  ``workspace`` is allocated with torch when not given."""
+    read.  ``workspace`` is allocated (zero-filled) with torch when not given; a workspace passed
+    in must have been zero-filled when it was allocated (its split counters are zero between
+    calls), and may then be reused for any batch."""
     import torch
     nb, bs, hkv, d = _pool_shape(k_cache, v_cache)
     B, hq, dq = (int(x) for x in q.shape)
@@ -236,7 +238,7 @@ def nv_paged_decode_attn(q, k_cache, v_cache, block_tables, context_lens, scale,
         out = torch.empty_like(q)
     ws_need = nv_paged_decode_workspace_size(B, hq, d, int(max_context_len))
     if workspace is None and ws_need:
-        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(ws_need, dtype=torch.uint8, device=q.device)   # split counters start at zero
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load_library().nv_paged_decode_attn(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.stride(0), _ptr(context_lens), B, hq,
@@ -267,7 +269,7 @@ def nv_store_decode_attn(q, k, v, slot_mapping, k_cache, v_cache, block_tables, 
         out = torch.empty_like(q)
     ws_need = nv_paged_decode_workspace_size(B, hq, d, int(max_context_len))
     if workspace is None and ws_need:
-        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(ws_need, dtype=torch.uint8, device=q.device)   # split counters start at zero
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = load_library().nv_store_decode_attn(
         _ptr(q), _ptr(k), k.stride(0), _ptr(v), v.stride(0), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),

@@ -22,8 +22,9 @@
 //     weights then stay below 2^8 and the accumulation in fp32 is unaffected.
 //   * HBM-bound (about 4 flop per byte of KV), so no tensor cores: fp32 FMAs on CUDA cores.
 //   * A sequence split over several CTAs writes unnormalised partial outputs plus its
-//     (max, sum); a small merge kernel combines them.  Single-split sequences write bf16
-//     output directly.
+//     (max, sum); the sequence's last CTA to finish (a per-sequence counter in the workspace)
+//     combines them and writes the bf16 output, so no separate merge pass runs.  Single-split
+//     sequences write bf16 output directly.
 //   * nv_store_decode_attn (the store of the same forward fused in; kFused): the CTA whose
 //     split holds position L-1 copies the new K/V row from the inputs into its last staged
 //     chunk instead of from the pool, and its consumer warps write that row to its slot.
@@ -39,6 +40,10 @@ constexpr int kD = 128;           // head_dim
 constexpr int kT = 8;             // positions per staged chunk
 constexpr int kStages = 3;        // chunks in flight per CTA
 constexpr float kRescaleLog2 = 8.0f;
+// Split counters sit at the start of the workspace in a region of fixed size, so a workspace
+// reused for batches of different sizes keeps them in place (they are zero between calls).
+constexpr int kMaxCountedSeqs = 65536;
+constexpr size_t kCounterBytes = (size_t)kMaxCountedSeqs * sizeof(int32_t);
 
 struct DecodeParams {
     const __nv_bfloat16 *q;
@@ -49,6 +54,7 @@ struct DecodeParams {
     __nv_bfloat16 *out;
     float *part_o;      // [num_seqs, max_splits, Hq, 128]
     float *part_ml;     // [num_seqs, max_splits, Hq, 2]
+    int32_t *split_done;  // [num_seqs]: splits finished in this call; zero between calls
     int32_t *d_err;
     int32_t bt_stride;
     int32_t num_q_heads;
@@ -110,6 +116,39 @@ __device__ __forceinline__ void unpack8(const uint4 &r, float (&f)[8])
     f[5] = bf16hi(r.z);
     f[6] = bf16lo(r.w);
     f[7] = bf16hi(r.w);
+}
+
+// Combine the partial results of a sequence that was split: o = sum_s 2^(m_s-M) o_s /
+// sum_s 2^(m_s-M) l_s.  Run by the sequence's last CTA, a thread owning 4 dims of one head at a
+// time.  The partials were written by other CTAs in this call: read them from L2 (.cg), past this
+// SM's L1.
+__device__ __forceinline__ void merge_splits(const DecodeParams &p, int b, int nsplit, int tid, int nthreads)
+{
+    const int items = p.num_q_heads * (kD / 4);
+    for (int it = tid; it < items; it += nthreads) {
+        const int h = it / (kD / 4);
+        const int d4 = it % (kD / 4);
+        float M = -INFINITY;
+        for (int s = 0; s < nsplit; ++s)
+            M = fmaxf(M, __ldcg(p.part_ml + (((size_t)b * p.max_splits + s) * p.num_q_heads + h) * 2));
+        float den = 0.f, n0 = 0.f, n1 = 0.f, n2 = 0.f, n3 = 0.f;
+        for (int s = 0; s < nsplit; ++s) {
+            const size_t unit = (size_t)b * p.max_splits + s;
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml + (unit * p.num_q_heads + h) * 2));
+            const float w = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
+            const float4 o = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (unit * p.num_q_heads + h) * kD + d4 * 4));
+            den = fmaf(w, ml.y, den);
+            n0 = fmaf(w, o.x, n0);
+            n1 = fmaf(w, o.y, n1);
+            n2 = fmaf(w, o.z, n2);
+            n3 = fmaf(w, o.w, n3);
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        uint2 w2;
+        w2.x = pack_bf16x2(n0 * inv, n1 * inv);
+        w2.y = pack_bf16x2(n2 * inv, n3 * inv);
+        *reinterpret_cast<uint2 *>(p.out + ((size_t)b * p.num_q_heads + h) * kD + d4 * 4) = w2;
+    }
 }
 
 template <int G, int MAX_KV_HEADS, bool kFused>
@@ -406,43 +445,26 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
                         make_float2(m_g[g], l_g[g]);
             }
         }
-    }
-}
-
-// Combine the partial results of sequences that were split: o = sum_s 2^(m_s-M) o_s /
-// sum_s 2^(m_s-M) l_s.  One CTA per sequence; a thread owns 4 dims of one head.
-__global__ void __launch_bounds__(256) merge_splits_kernel(const DecodeParams p)
-{
-    const int b = blockIdx.x;
-    int L = __ldg(p.context_lens + b);
-    L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
-    const int nsplit = (L + p.split_tokens - 1) / p.split_tokens;
-    if (nsplit <= 1)
-        return;
-    const int items = p.num_q_heads * (kD / 4);
-    for (int it = threadIdx.x; it < items; it += blockDim.x) {
-        const int h = it / (kD / 4);
-        const int d4 = it % (kD / 4);
-        float M = -INFINITY;
-        for (int s = 0; s < nsplit; ++s)
-            M = fmaxf(M, p.part_ml[(((size_t)b * p.max_splits + s) * p.num_q_heads + h) * 2]);
-        float den = 0.f, n0 = 0.f, n1 = 0.f, n2 = 0.f, n3 = 0.f;
-        for (int s = 0; s < nsplit; ++s) {
-            const size_t unit = (size_t)b * p.max_splits + s;
-            const float2 ml = *reinterpret_cast<const float2 *>(p.part_ml + (unit * p.num_q_heads + h) * 2);
-            const float w = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - M);
-            const float4 o = *reinterpret_cast<const float4 *>(p.part_o + (unit * p.num_q_heads + h) * kD + d4 * 4);
-            den = fmaf(w, ml.y, den);
-            n0 = fmaf(w, o.x, n0);
-            n1 = fmaf(w, o.y, n1);
-            n2 = fmaf(w, o.z, n2);
-            n3 = fmaf(w, o.w, n3);
+        // Count this split as done (its partials made visible first); the sequence's last split
+        // to get here merges them all.  Every CTA with t0 < L reaches this point exactly once,
+        // whatever happened in its loop, so the counter always reaches nsplit and is reset.
+        // (The barrier orders the warps' partial stores before thread 0's fence, which makes them
+        // visible device-wide before its count; on the last split, the fence after the count
+        // orders the merge's reads after every other split's partials.)
+        __shared__ int s_last;
+        const uint32_t consumers = (uint32_t)hkv * 32u;
+        asm volatile("bar.sync 1, %0;" ::"r"(consumers) : "memory");
+        if (threadIdx.x == 0) {
+            __threadfence();
+            s_last = atomicAdd(p.split_done + b, 1) == nsplit - 1;
+            __threadfence();
         }
-        const float inv = den > 0.f ? 1.f / den : 0.f;
-        uint2 w2;
-        w2.x = pack_bf16x2(n0 * inv, n1 * inv);
-        w2.y = pack_bf16x2(n2 * inv, n3 * inv);
-        *reinterpret_cast<uint2 *>(p.out + ((size_t)b * p.num_q_heads + h) * kD + d4 * 4) = w2;
+        asm volatile("bar.sync 1, %0;" ::"r"(consumers) : "memory");
+        if (s_last) {
+            merge_splits(p, b, nsplit, (int)threadIdx.x, (int)consumers);
+            if (threadIdx.x == 0)
+                p.split_done[b] = 0;      // ready for the next call
+        }
     }
 }
 
@@ -468,14 +490,7 @@ int launch_decode(const DecodeParams &p, int num_seqs, size_t smem_bytes, cudaSt
     }
     dim3 grid(num_seqs, p.max_splits);
     paged_decode_kernel<G, MAXH, kFused><<<grid, (p.num_kv_heads + 1) * 32, smem_bytes, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess)
-        return NV_ERR_CUDA;
-    if (p.max_splits > 1) {
-        merge_splits_kernel<<<num_seqs, 256, 0, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess)
-            return NV_ERR_CUDA;
-    }
-    return NV_OK;
+    return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
 
 template <int MAXH, bool kFused>
@@ -511,7 +526,7 @@ extern "C" size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q
     const int max_splits = (max_context_len + split - 1) / split;
     if (max_splits <= 1)
         return 0;
-    return (size_t)num_seqs * max_splits * num_q_heads * (kD + 2) * sizeof(float);
+    return kCounterBytes + (size_t)num_seqs * max_splits * num_q_heads * (kD + 2) * sizeof(float);
 }
 
 namespace {
@@ -594,7 +609,10 @@ int decode_entry(const void *q, const void *k_cache, const void *v_cache, const 
         const size_t need = nv_paged_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len);
         if (!workspace || workspace_bytes < need || !aligned16(workspace))
             return NV_ERR_WORKSPACE;
-        p.part_o = static_cast<float *>(workspace);
+        if (num_seqs > kMaxCountedSeqs)
+            return NV_ERR_UNSUPPORTED;
+        p.split_done = static_cast<int32_t *>(workspace);
+        p.part_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kCounterBytes);
         p.part_ml = p.part_o + (size_t)num_seqs * p.max_splits * num_q_heads * kD;
     }
     const size_t smem = (size_t)kStages * 2 * kT * num_kv_heads * kD * 2 + 2 * kStages * 8 + kStages * 4 + 16;
@@ -640,30 +658,33 @@ extern "C" int nv_store_decode_attn(const void *q, const void *k, int64_t k_row_
 // the process exits.
 // ---------------------------------------------------------------------------------------
 static __device__ __align__(256) unsigned char g_decode_scratch[NV_DECODE_STATIC_SCRATCH_BYTES];
+// split counters of the allocation-free path: zero at load, and every call leaves them zero
+static __device__ int32_t g_decode_split_done[kMaxCountedSeqs];
 
 namespace {
 
-// Device address of g_decode_scratch on the current device.  Looked up once per device (the
-// host-side name is only a stand-in for the device array, never an address to pass a kernel).
-void *static_scratch(int *status)
+// Device addresses of g_decode_scratch and g_decode_split_done on the current device.  Looked
+// up once per device (the host-side names are only stand-ins for the device arrays, never
+// addresses to pass a kernel).
+bool static_arrays(void **scratch, int32_t **split_done)
 {
     static std::mutex mu;
-    static void *addr[64];
+    static void *addr[64][2];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-        *status = NV_ERR_CUDA;
-        return nullptr;
-    }
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return false;
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || !ptr) {
-            *status = NV_ERR_CUDA;
-            return nullptr;
-        }
-        addr[dev] = ptr;
+    if (!addr[dev][0] || !addr[dev][1]) {
+        void *a = nullptr, *c = nullptr;
+        if (cudaGetSymbolAddress(&a, g_decode_scratch) != cudaSuccess || !a ||
+            cudaGetSymbolAddress(&c, g_decode_split_done) != cudaSuccess || !c)
+            return false;
+        addr[dev][0] = a;
+        addr[dev][1] = c;
     }
-    return addr[dev];
+    *scratch = addr[dev][0];
+    *split_done = static_cast<int32_t *>(addr[dev][1]);
+    return true;
 }
 
 }  // namespace
@@ -730,12 +751,13 @@ extern "C" int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, 
     p.max_splits = (max_len + split - 1) / split;
     p.scale_log2 = scale * nvkv::kLog2e;
     if (p.max_splits > 1) {
-        int status = NV_OK;
-        void *scratch = static_scratch(&status);
-        if (!scratch)
-            return status;
+        if (num_seqs > kMaxCountedSeqs)
+            return NV_ERR_UNSUPPORTED;
+        void *scratch = nullptr;
+        if (!static_arrays(&scratch, &p.split_done))
+            return NV_ERR_CUDA;
         // Every partial the merge reads is written earlier in the same call, so nothing in the
-        // array has to start at zero.
+        // scratch array has to start at zero; the counters are zero between calls.
         p.part_o = static_cast<float *>(scratch);
         p.part_ml = p.part_o + (size_t)num_seqs * p.max_splits * num_q_heads * kD;
     }
