@@ -281,7 +281,7 @@ def run_ours(args, rank, world, local_rank):
         if ev is not None:
             ev[1].record(stream)
 
-    launches_per_decode_step = 1 + 1 + (1 if ws_bytes > 0 else 0)
+    launches_per_decode_step = 2        # store, then decode (split merge inside the decode kernel)
 
     sampler = ClockSampler(local_rank)
     sampler.__enter__()
@@ -567,7 +567,7 @@ def run_ours(args, rank, world, local_rank):
         "hbm_frac_of_peak": round(value / hbm_peak, 4),
         "attended_tok_s": round(tok_total / (dec_ms_max * 1e-3), 1),
         "roofline": {
-            "kernel": "paged_decode_kernel + merge_splits_kernel (nv_paged_decode_attn)",
+            "kernel": "paged_decode_kernel, split merge fused in (nv_paged_decode_attn)",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4),
             "peak_source": f"{pk_kind} hbm_gbs",
@@ -579,7 +579,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms_max / args.steps, 4)},
         "fused_store_decode": {
-            "kernel": "paged_decode_kernel<4, 8, fused> + merge_splits_kernel (nv_store_decode_attn)",
+            "kernel": "paged_decode_kernel<4, 8, fused> (nv_store_decode_attn)",
             "value": round(kv_total / (fused_ms_max * 1e-3) / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(fused_ms_max / args.steps, 4),
             "separate_ms_per_step": round(dec_ms_max / args.steps, 4),
@@ -607,9 +607,11 @@ def run_ours(args, rank, world, local_rank):
         },
         "gpu_launches": launches_per_decode_step * args.steps,
         "gpu_launches_note": "kernels of this library launched in the headline timed region (store + split-KV decode "
-                             "+ merge per step); all timed phases together: see gpu_launches_all_phases",
-        "gpu_launches_all_phases": (launches_per_decode_step * 2 + (launches_per_decode_step - 1) + 1 + 2 + 3 + 1)
-                                   * args.steps,
+                             "per step); all timed phases together: see gpu_launches_all_phases",
+        # per step: headline and e2e (store + decode each), fused (1), prepare_decode (1), sampler (2), prefill
+        # (store + pre-pass + attention), prologue (1); then the decode call of the three extra configs
+        "gpu_launches_all_phases": (launches_per_decode_step * 2 + 1 + 1 + 2 + 3 + 1) * args.steps
+                                   + 3 * max(5, min(args.steps, 50)),
         "clocks": clocks,
         "prefill": {
             "workload": "chunked prefill with prefix cache (store 16384 new rows + causal varlen prefill): 16 seqs, "
@@ -770,8 +772,9 @@ def run_profile_case(case: str):
     """Run one small case three times (store + attention) for an ncu capture, then exit.
 
     decode-64seq: the first 64 sequences' shapes of the Qwen3-8B decode batch (about 0.7 GB of
-    KV, above the 129 MB L2, a few GB on the device in all); prefill-chunk: the full
-    chunked-prefill workload (about 0.3 GB)."""
+    KV, above the 129 MB L2, a few GB on the device in all); decode-512seq: the headline batch
+    itself (for one-pass DRAM counters only); prefill-chunk: the full chunked-prefill workload
+    (about 0.3 GB)."""
     import torch
 
     import paged_kv_attention_store_gb300 as nv
@@ -799,6 +802,8 @@ def run_profile_case(case: str):
     if case == "decode-64seq":
         ctx = np.random.default_rng([0, 200]).integers(1024, 4097, size=512)[:64]
         b = W.make_decode("qwen3-8b-decode-64", 0, ctx, 32, 8, 128, 256)
+    elif case == "decode-512seq":
+        b = W.qwen8_decode(seed=0)     # the headline batch (about 13 GB on the device)
     elif case.startswith("shared-prefix-bs"):
         b = W.shared_prefix(block_size=int(case[len("shared-prefix-bs"):]))
     else:
@@ -844,7 +849,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work per oracle baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seqs-per-step", type=int, default=1)
-    ap.add_argument("--profile-case", choices=["decode-64seq", "prefill-chunk", "prologue-chunk", "sampler-256rows",
+    ap.add_argument("--profile-case", choices=["decode-64seq", "decode-512seq", "prefill-chunk", "prologue-chunk",
+                                               "sampler-256rows",
                                                "shared-prefix-bs256", "shared-prefix-bs16"],
                     help="run one small case three times for an ncu capture and exit")
     args = ap.parse_args()
