@@ -147,3 +147,33 @@ def test_decode_length_beyond_hint_is_flagged():
     db = DeviceBatch(b)
     db.decode(max_context_len=100)
     assert db.err() & nv.NV_DERR_LENGTH
+
+
+def test_decode_workspace_reused_across_batches_and_after_an_error():
+    """One zero-filled workspace serves calls of different batch sizes and split counts, including one
+    right after a call that flagged a bad block id: the per-sequence split counters the merge uses are
+    left at zero by every call, so each call still matches the oracle."""
+    import torch
+    import paged_kv_attention_store_gb300 as nv
+    from tests.gpu_util import oracle_cache_after_store, oracle_decode
+    orc = oracle.default()
+    rng = np.random.default_rng(27)
+    big = W.make_decode("reuse-big", 27, rng.integers(1, 4097, 200).tolist(), 32, 8, 128, 64)
+    small = W.make_decode("reuse-small", 28, [4096, 3000, 17, 2500], 32, 8, 128, 64)
+    ws = torch.zeros(max(nv.nv_paged_decode_workspace_size(b.num_seqs, 32, 128, 4096) for b in (big, small)),
+                     dtype=torch.uint8, device="cuda")
+    bad_bt = small.block_tables.copy()
+    bad_bt[1, 3] = small.num_blocks + 5
+    bad = W.PagedBatch(**{**small.__dict__, "block_tables": bad_bt})
+    for b, expect_err in ((big, False), (small, False), (bad, True), (small, False), (big, False)):
+        db = DeviceBatch(b)
+        db.store()
+        got = nv.nv_paged_decode_attn(db.q, db.k_cache, db.v_cache, db.block_tables, db.seq_lens, b.scale,
+                                      max_context_len=4096, workspace=ws, d_err=db.d_err)
+        err = db.err()
+        if expect_err:
+            assert err & nv.NV_DERR_BLOCK_RANGE
+            continue
+        assert err == 0
+        kc, vc = oracle_cache_after_store(orc, b, db.kc_host0, db.vc_host0)
+        compare(host_f32(got), oracle_decode(orc, b, kc, vc), f"reused workspace {b.name}")
