@@ -87,6 +87,19 @@ def test_decode_validation(lib):
     assert lib.nv_paged_decode_workspace_size(4, 32, 128, 64) == 0   # one split: no workspace
 
 
+def test_decode_workspace_size_follows_the_split_rule(lib):
+    """256 KiB of split counters, then num_seqs x splits x Hq x (128 + 2) floats of partials; the
+    split is 512 positions halved while the batch has fewer than 1200 units, stopping at 256 once
+    it has 600 (and at 64 at the least)."""
+    def size(B, L, hq=32):
+        return lib.nv_paged_decode_workspace_size(B, hq, 128, L)
+    part = lambda B, splits, hq=32: 256 * 1024 + B * splits * hq * 130 * 4
+    assert size(512, 4096) == part(512, 8)        # 4096 units at 512 positions
+    assert size(256, 2048, 16) == part(256, 8, 16)  # 1024 units at 512 -> 2048 at 256
+    assert size(64, 4096) == part(64, 16)         # 512 -> 1024 units at 256: stop (>= 600)
+    assert size(4, 4096) == part(4, 64)           # a tiny batch goes down to 64 positions
+
+
 def _fused(lib, q=FAKE, k=FAKE, ks=1024, v=FAKE, vs=1024, sm=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, bts=16, cl=FAKE, B=4,
            hq=32, hkv=8, d=128, bs=256, nb=64, maxc=256, out=FAKE):
     return lib.nv_store_decode_attn(q, k, ks, v, vs, sm, kc, vc, bt, bts, cl, B, hq, hkv, d, bs, nb, maxc, 0.088, out,
