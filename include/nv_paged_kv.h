@@ -299,11 +299,12 @@ int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, const void 
  *   k_cache, v_cache  as above; additionally num_blocks*block_size < 2^31.
  *   workspace     device scratch of at least nv_paged_prefill_workspace_size(...) bytes,
  *                 16-byte aligned, else NV_ERR_WORKSPACE.  The call first writes into it (on
- *                 `stream`, a one-CTA pre-pass) the list of query tiles, heaviest first, and the
- *                 counter from which the persistent CTAs claim them, so it needs no
+ *                 `stream`, a one-CTA pre-pass) the list of query tiles -- sequence by
+ *                 sequence, heaviest sequence first, each sequence's tiles heaviest first -- and
+ *                 the counter from which the persistent CTAs claim them, so it needs no
  *                 initialisation; calls that share a workspace must not overlap on the device.
  *                 A batch whose tiles would not fit (cu_seqlens_q inconsistent with total_q) sets
- *                 NV_DERR_LENGTH and leaves the lightest tiles uncomputed.
+ *                 NV_DERR_LENGTH and leaves the last-listed tiles uncomputed.
  * Enqueues two kernels: the pre-pass and the attention kernel.
  */
 
