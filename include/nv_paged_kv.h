@@ -61,7 +61,8 @@ typedef enum nv_status {
 #define NV_DERR_LENGTH 0x4        /* a length exceeds the block table, the host hint, or is negative */
 #define NV_DERR_TIMEOUT 0x8       /* a bounded wait on an asynchronous copy gave up */
 #define NV_DERR_SLOT_MISMATCH 0x10 /* fused store + decode: a slot that is not position L-1's (row not stored) */
-#define NV_DERR_VALUE 0x20         /* sampler: a temperature that is not positive and finite (token -1) */
+#define NV_DERR_VALUE 0x20         /* sampler: a temperature that is not positive and finite (token -1);
+                                      decode: a split counter of the workspace was not zero */
 
 /* Human-readable name of an nv_status value (static string). */
 const char *nv_status_string(int status);
@@ -206,7 +207,9 @@ size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
  *                 (may be NULL when that size is 0), 16-byte aligned.  Its first 256 KiB hold
  *                 the per-sequence split counters: they must be ZERO before the first call
  *                 that uses the workspace (allocate it zero-filled), and every call leaves them
- *                 zero, whatever the batch; the rest needs no initialisation.  Calls that share
+ *                 zero, whatever the batch; the rest needs no initialisation.  A counter found
+ *                 outside [0, splits) sets NV_DERR_VALUE (that sequence's output is then not
+ *                 trustworthy, and the workspace must be zero-filled again).  Calls that share
  *                 a workspace must not overlap on the device.  Batches of more than 65536
  *                 sequences whose contexts need several splits return NV_ERR_UNSUPPORTED.
  */

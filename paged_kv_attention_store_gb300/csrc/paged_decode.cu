@@ -456,7 +456,10 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
         asm volatile("bar.sync 1, %0;" ::"r"(consumers) : "memory");
         if (threadIdx.x == 0) {
             __threadfence();
-            s_last = atomicAdd(p.split_done + b, 1) == nsplit - 1;
+            const int prev = atomicAdd(p.split_done + b, 1);
+            s_last = prev == nsplit - 1;
+            if (prev < 0 || prev >= nsplit)
+                flag_error(p.d_err, NV_DERR_VALUE);   // the counters were not zero: workspace not zero-filled
             __threadfence();
         }
         asm volatile("bar.sync 1, %0;" ::"r"(consumers) : "memory");

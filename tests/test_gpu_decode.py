@@ -177,3 +177,17 @@ def test_decode_workspace_reused_across_batches_and_after_an_error():
         assert err == 0
         kc, vc = oracle_cache_after_store(orc, b, db.kc_host0, db.vc_host0)
         compare(host_f32(got), oracle_decode(orc, b, kc, vc), f"reused workspace {b.name}")
+
+
+def test_decode_workspace_not_zero_filled_is_flagged():
+    """Split counters that do not start at zero (a workspace that was not zero-filled) are reported."""
+    import torch
+    import paged_kv_attention_store_gb300 as nv
+    b = W.make_decode("dirty-ws", 29, [4096, 3000, 2500], 32, 8, 128, 64)
+    db = DeviceBatch(b)
+    db.store()
+    ws = torch.full((nv.nv_paged_decode_workspace_size(b.num_seqs, 32, 128, 4096),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    nv.nv_paged_decode_attn(db.q, db.k_cache, db.v_cache, db.block_tables, db.seq_lens, b.scale,
+                            max_context_len=4096, workspace=ws, d_err=db.d_err)
+    assert db.err() & nv.NV_DERR_VALUE
