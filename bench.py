@@ -772,7 +772,8 @@ def run_profile_case(case: str):
     """Run one small case three times (store + attention) for an ncu capture, then exit.
 
     decode-64seq: the first 64 sequences' shapes of the Qwen3-8B decode batch (about 0.7 GB of
-    KV, above the 129 MB L2, a few GB on the device in all); decode-512seq: the headline batch
+    KV, above the 129 MB L2, a few GB on the device in all); decode-g8-64seq: the same lengths with
+    64 query heads over the 8 kv heads (Qwen3-32B's attention shape, group 8); decode-512seq: the headline batch
     itself (for one-pass DRAM counters only); prefill-chunk: the full chunked-prefill workload
     (about 0.3 GB)."""
     import torch
@@ -802,6 +803,9 @@ def run_profile_case(case: str):
     if case == "decode-64seq":
         ctx = np.random.default_rng([0, 200]).integers(1024, 4097, size=512)[:64]
         b = W.make_decode("qwen3-8b-decode-64", 0, ctx, 32, 8, 128, 256)
+    elif case == "decode-g8-64seq":
+        ctx = np.random.default_rng([0, 200]).integers(1024, 4097, size=512)[:64]
+        b = W.make_decode("group8-decode-64", 0, ctx, 64, 8, 128, 256)
     elif case == "decode-512seq":
         b = W.qwen8_decode(seed=0)     # the headline batch (about 13 GB on the device)
     elif case.startswith("shared-prefix-bs"):
@@ -849,7 +853,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work per oracle baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seqs-per-step", type=int, default=1)
-    ap.add_argument("--profile-case", choices=["decode-64seq", "decode-512seq", "prefill-chunk", "prologue-chunk",
+    ap.add_argument("--profile-case", choices=["decode-64seq", "decode-g8-64seq", "decode-512seq", "prefill-chunk", "prologue-chunk",
                                                "sampler-256rows",
                                                "shared-prefix-bs256", "shared-prefix-bs16"],
                     help="run one small case three times for an ncu capture and exit")

@@ -10,10 +10,12 @@
 //     ALL kv heads of its unit, so each position's K (and V) row of Hkv*128 bf16 values is
 //     one contiguous run in the pool, and T consecutive positions inside a block are one
 //     contiguous run of T*Hkv*256 bytes: a single 1-D TMA bulk copy moves them into shared
-//     memory, completing on an mbarrier.  A producer warp keeps kStages such chunks in
+//     memory, completing on an mbarrier.  A producer warp keeps three such chunks in
 //     flight per CTA (two CTAs per SM), reading one block-table entry per block.
 //   * Consumer warp w owns kv head w and its G = Hq/Hkv query heads, so every K/V element
-//     is read from shared memory once and used G times (GQA sharing).  A half-warp handles
+//     is read from shared memory once and used G times (GQA sharing).  At G = 8 two warps
+//     share a kv head, four query heads each, and the CTA (one per SM) keeps six chunks in
+//     flight.  A half-warp handles
 //     one position at a time, each lane 8 of the 128 dims; partial dot products are reduced
 //     with a reduce-scatter over 4 shuffle levels that leaves each lane the full score of
 //     one of the G heads, so the exponential is computed once per (position, head).
@@ -38,7 +40,6 @@ using namespace nvkv;
 
 constexpr int kD = 128;           // head_dim
 constexpr int kT = 8;             // positions per staged chunk
-constexpr int kStages = 3;        // chunks in flight per CTA
 constexpr float kRescaleLog2 = 8.0f;
 // Split counters sit at the start of the workspace in a region of fixed size, so a workspace
 // reused for batches of different sizes keeps them in place (they are zero between calls).
@@ -106,16 +107,12 @@ __device__ __forceinline__ float reduce_to_owner(const float (&x)[G], int sl)
     return v[0];
 }
 
-__device__ __forceinline__ void unpack8(const uint4 &r, float (&f)[8])
+__device__ __forceinline__ void unpack8(const uint4 &r, float2 (&f)[4])
 {
-    f[0] = bf16lo(r.x);
-    f[1] = bf16hi(r.x);
-    f[2] = bf16lo(r.y);
-    f[3] = bf16hi(r.y);
-    f[4] = bf16lo(r.z);
-    f[5] = bf16hi(r.z);
-    f[6] = bf16lo(r.w);
-    f[7] = bf16hi(r.w);
+    f[0] = make_float2(bf16lo(r.x), bf16hi(r.x));
+    f[1] = make_float2(bf16lo(r.y), bf16hi(r.y));
+    f[2] = make_float2(bf16lo(r.z), bf16hi(r.z));
+    f[3] = make_float2(bf16lo(r.w), bf16hi(r.w));
 }
 
 // Combine the partial results of a sequence that was split: o = sum_s 2^(m_s-M) o_s /
@@ -151,10 +148,35 @@ __device__ __forceinline__ void merge_splits(const DecodeParams &p, int b, int n
     }
 }
 
-template <int G, int MAX_KV_HEADS, bool kFused>
-__global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 2 : 1))
+// Consumer warps per kv head: with 8 query heads per kv head, two warps split them (4 each) and
+// share every staged K/V element, so a warp's per-position work stays that of a group of 4 (one
+// warp holding all 8 measured 2.75x slower: its FMA work doubled and its registers spilled).
+__host__ __device__ constexpr int decode_warps_per_kv_head(int group, int max_kv_heads)
+{
+    return (group == 8 && max_kv_heads <= 8) ? 2 : 1;
+}
+
+// Chunks in flight per CTA.  Three stages of 8 kv heads take 96 KB, so two CTAs share an SM; a
+// CTA with two warps per kv head has too many registers for a second CTA on its SM, so it keeps
+// six stages (192 KB) in flight by itself.
+__host__ __device__ constexpr int decode_stages(int group, int max_kv_heads)
+{
+    return decode_warps_per_kv_head(group, max_kv_heads) == 2 ? 6 : 3;
+}
+
+__host__ __device__ constexpr size_t decode_smem_bytes(int stages, int num_kv_heads)
+{
+    return (size_t)stages * 2 * kT * num_kv_heads * kD * 2 + 2 * stages * 8 + stages * 4 + 16;
+}
+
+template <int GQ, int MAX_KV_HEADS, bool kFused>
+__global__ void __launch_bounds__((MAX_KV_HEADS * decode_warps_per_kv_head(GQ, MAX_KV_HEADS) + 1) * 32,
+                                  (MAX_KV_HEADS <= 8 && decode_warps_per_kv_head(GQ, MAX_KV_HEADS) == 1 ? 2 : 1))
     paged_decode_kernel(const DecodeParams p)
 {
+    constexpr int kWPH = decode_warps_per_kv_head(GQ, MAX_KV_HEADS);   // consumer warps per kv head
+    constexpr int G = GQ / kWPH;                                        // query heads per consumer warp
+    constexpr int kS = decode_stages(GQ, MAX_KV_HEADS);                 // chunks in flight
     extern __shared__ __align__(128) uint8_t smem[];
     const int hkv = p.num_kv_heads;
     const int dkv = hkv * kD;                        // elements per pool row
@@ -209,28 +231,28 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
     const int nsplit = (L + p.split_tokens - 1) / p.split_tokens;
     const int nchunks = (t1 - t0 + kT - 1) / kT;
 
-    // shared memory: [kStages][K chunk | V chunk], then barriers and per-stage valid counts
+    // shared memory: [kS][K chunk | V chunk], then barriers and per-stage valid counts
     const uint32_t stage_bytes = 2 * chunk_bytes;
-    uint8_t *tail = smem + (size_t)kStages * stage_bytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(tail);   // full[kStages], empty[kStages]
-    int32_t *valid_rows = reinterpret_cast<int32_t *>(tail + 2 * kStages * sizeof(uint64_t));
+    uint8_t *tail = smem + (size_t)kS * stage_bytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tail);   // full[kS], empty[kS]
+    int32_t *valid_rows = reinterpret_cast<int32_t *>(tail + 2 * kS * sizeof(uint64_t));
     const uint32_t smem_base = smem_u32(smem);
     const uint32_t bar_base = smem_u32(bars);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kS; ++s) {
             mbar_init(bar_base + 8 * s, 1);                    // full: producer arrive + tx bytes
-            mbar_init(bar_base + 8 * (kStages + s), hkv);      // empty: one arrive per consumer warp
+            mbar_init(bar_base + 8 * (kS + s), hkv * kWPH);   // empty: one arrive per consumer warp
         }
         fence_barrier_init();
     }
     // Rows a partial chunk does not copy keep stale-but-finite values (zero at first).
-    for (uint32_t i = threadIdx.x; i < (uint32_t)kStages * stage_bytes / 16; i += blockDim.x)
+    for (uint32_t i = threadIdx.x; i < (uint32_t)kS * stage_bytes / 16; i += blockDim.x)
         sts_u4(smem_base + 16 * i, make_uint4(0, 0, 0, 0));
     fence_proxy_async_smem();   // the zeros must land before any bulk copy writes these bytes
     __syncthreads();
 
-    if (warp == hkv) {
+    if (warp == hkv * kWPH) {
         // ---------------- producer: one lane issues the bulk copies ----------------
         if (lane == 0) {
             const int bs_mask = (1 << p.block_shift) - 1;
@@ -240,8 +262,8 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
             bool blk_ok = false;
             int issued = 0;
             for (int c = 0; c < nchunks; ++c) {
-                const int s = c % kStages;
-                if (c >= kStages && !mbar_wait(bar_base + 8 * (kStages + s), ((c / kStages) - 1) & 1)) {
+                const int s = c % kS;
+                if (c >= kS && !mbar_wait(bar_base + 8 * (kS + s), ((c / kS) - 1) & 1)) {
                     flag_error(p.d_err, NV_DERR_TIMEOUT);
                     break;
                 }
@@ -282,34 +304,38 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
                 issued = c + 1;
             }
             // Do not leave while copies still land in this CTA's shared memory.
-            for (int c = max(0, issued - kStages); c < issued; ++c)
-                mbar_wait(bar_base + 8 * (c % kStages), (c / kStages) & 1);
+            for (int c = max(0, issued - kS); c < issued; ++c)
+                mbar_wait(bar_base + 8 * (c % kS), (c / kS) & 1);
         }
         return;
     }
 
-    // ---------------- consumers: warp w = kv head w, its G query heads ----------------
-    const int kvh = warp;
+    // ------- consumers: warp w = kv head w / kWPH, G of its query heads (share w % kWPH) -------
+    const int kvh = warp / kWPH;
+    const int hsub = warp % kWPH;
     const int half = lane >> 4;
     const int sl = lane & 15;
     constexpr int kLanesPerHead = 16 / G;
-    const int head0 = kvh * G;
+    const int head0 = kvh * GQ + hsub * G;
 
-    float qf[G][8];
+    // Dims are held in pairs and the dot products and accumulations use the packed fp32 pair
+    // instructions: each one does the FMAs of two dims.
+    const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
+    float2 qf[G][4];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         const uint4 r = *reinterpret_cast<const uint4 *>(p.q + ((size_t)b * p.num_q_heads + head0 + g) * kD + sl * 8);
         unpack8(r, qf[g]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            qf[g][i] *= p.scale_log2;
+        for (int i = 0; i < 4; ++i)
+            qf[g][i] = __fmul2_rn(qf[g][i], scale2);
     }
-    float acc[G][8];
+    float2 acc2[G][4];
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            acc[g][i] = 0.f;
+        for (int i = 0; i < 4; ++i)
+            acc2[g][i] = make_float2(0.f, 0.f);
     float m_run = -INFINITY;   // running max (log2 units) of head own_g, this half's positions
     float l_run = 0.f;         // running sum of weights of head own_g
 
@@ -318,8 +344,8 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
     const uint32_t row_bytes = (uint32_t)dkv * 2;
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
-        const int s = c % kStages;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_base + 8 * s, (c / kStages) & 1))) {
+        const int s = c % kS;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_base + 8 * s, (c / kS) & 1))) {
             if (lane == 0)
                 flag_error(p.d_err, NV_DERR_TIMEOUT);
             ok = false;
@@ -333,16 +359,16 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
 #pragma unroll
         for (int jj = 0; jj < kT / 2; ++jj) {
             const int j = half * (kT / 2) + jj;
-            float kf[8];
+            float2 kf[4];
             unpack8(lds_u4(kbase + j * row_bytes), kf);
             float part[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                float a = 0.f;
+                float2 a = __fmul2_rn(qf[g][0], kf[0]);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    a = fmaf(qf[g][i], kf[i], a);
-                part[g] = a;
+                for (int i = 1; i < 4; ++i)
+                    a = __ffma2_rn(qf[g][i], kf[i], a);
+                part[g] = a.x + a.y;
             }
             const float full = reduce_to_owner<G>(part, sl);
             sc[jj] = (j < nvalid) ? full : -INFINITY;
@@ -360,9 +386,10 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float a = __shfl_sync(0xffffffffu, alpha, (half << 4) + g * kLanesPerHead);
+                const float2 a2 = make_float2(a, a);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    acc[g][i] *= a;
+                for (int i = 0; i < 4; ++i)
+                    acc2[g][i] = __fmul2_rn(acc2[g][i], a2);
             }
         }
         float pj[kT / 2];
@@ -374,18 +401,19 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
 #pragma unroll
         for (int jj = 0; jj < kT / 2; ++jj) {
             const int j = half * (kT / 2) + jj;
-            float vf[8];
+            float2 vf[4];
             unpack8(lds_u4(vbase + j * row_bytes), vf);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
                 const float pg = __shfl_sync(0xffffffffu, pj[jj], (half << 4) + g * kLanesPerHead);
+                const float2 pg2 = make_float2(pg, pg);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    acc[g][i] = fmaf(pg, vf[i], acc[g][i]);
+                for (int i = 0; i < 4; ++i)
+                    acc2[g][i] = __ffma2_rn(pg2, vf[i], acc2[g][i]);
             }
         }
         // fused store: this warp writes its kv head of the new row (K by lanes 0-15, V by 16-31)
-        if (kFused && new_pos >= t0 + c * kT && new_pos < t0 + c * kT + kT && nvalid > 0) {
+        if (kFused && hsub == 0 && new_pos >= t0 + c * kT && new_pos < t0 + c * kT + kT && nvalid > 0) {
             const int tok0 = t0 + c * kT;
             const uint32_t src = (half ? vbase : kbase) + (uint32_t)(new_pos - tok0) * row_bytes;
             __nv_bfloat16 *dst = (half ? p.v_cache_w : p.k_cache_w) + new_slot * dkv + kvh * kD + sl * 8;
@@ -393,10 +421,18 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
         }
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(bar_base + 8 * (kStages + s));
+            mbar_arrive(bar_base + 8 * (kS + s));
     }
 
     // ---- merge the two half-warps (they saw disjoint positions), then write ----
+    float acc[G][8];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc[g][2 * i] = acc2[g][i].x;
+            acc[g][2 * i + 1] = acc2[g][i].y;
+        }
     float m_g[G], l_g[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -452,7 +488,7 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, (MAX_KV_HEADS <= 8 ? 
         // visible device-wide before its count; on the last split, the fence after the count
         // orders the merge's reads after every other split's partials.)
         __shared__ int s_last;
-        const uint32_t consumers = (uint32_t)hkv * 32u;
+        const uint32_t consumers = (uint32_t)(hkv * kWPH) * 32u;
         asm volatile("bar.sync 1, %0;" ::"r"(consumers) : "memory");
         if (threadIdx.x == 0) {
             __threadfence();
@@ -486,8 +522,9 @@ int decode_split_tokens(int num_seqs, int max_context_len)
 }
 
 template <int G, int MAXH, bool kFused>
-int launch_decode(const DecodeParams &p, int num_seqs, size_t smem_bytes, cudaStream_t stream)
+int launch_decode(const DecodeParams &p, int num_seqs, cudaStream_t stream)
 {
+    const size_t smem_bytes = decode_smem_bytes(decode_stages(G, MAXH), p.num_kv_heads);
     static bool configured = false;   // benign race: every thread sets the same attribute value
     if (!configured) {
         if (cudaFuncSetAttribute(paged_decode_kernel<G, MAXH, kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -496,30 +533,31 @@ int launch_decode(const DecodeParams &p, int num_seqs, size_t smem_bytes, cudaSt
         configured = true;
     }
     dim3 grid(num_seqs, p.max_splits);
-    paged_decode_kernel<G, MAXH, kFused><<<grid, (p.num_kv_heads + 1) * 32, smem_bytes, stream>>>(p);
+    constexpr int wph = decode_warps_per_kv_head(G, MAXH);
+    paged_decode_kernel<G, MAXH, kFused><<<grid, (p.num_kv_heads * wph + 1) * 32, smem_bytes, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
 
 template <int MAXH, bool kFused>
-int dispatch_group(int group, const DecodeParams &p, int num_seqs, size_t smem, cudaStream_t st)
+int dispatch_group(int group, const DecodeParams &p, int num_seqs, cudaStream_t st)
 {
     switch (group) {
-    case 1: return launch_decode<1, MAXH, kFused>(p, num_seqs, smem, st);
-    case 2: return launch_decode<2, MAXH, kFused>(p, num_seqs, smem, st);
-    case 4: return launch_decode<4, MAXH, kFused>(p, num_seqs, smem, st);
-    case 8: return launch_decode<8, MAXH, kFused>(p, num_seqs, smem, st);
+    case 1: return launch_decode<1, MAXH, kFused>(p, num_seqs, st);
+    case 2: return launch_decode<2, MAXH, kFused>(p, num_seqs, st);
+    case 4: return launch_decode<4, MAXH, kFused>(p, num_seqs, st);
+    case 8: return launch_decode<8, MAXH, kFused>(p, num_seqs, st);
     default: return NV_ERR_UNSUPPORTED;
     }
 }
 
-int dispatch(int group, const DecodeParams &p, int num_seqs, size_t smem, cudaStream_t st)
+int dispatch(int group, const DecodeParams &p, int num_seqs, cudaStream_t st)
 {
     const bool fused = p.k_new != nullptr;
     if (p.num_kv_heads <= 8)
-        return fused ? dispatch_group<8, true>(group, p, num_seqs, smem, st)
-                     : dispatch_group<8, false>(group, p, num_seqs, smem, st);
-    return fused ? dispatch_group<16, true>(group, p, num_seqs, smem, st)
-                 : dispatch_group<16, false>(group, p, num_seqs, smem, st);
+        return fused ? dispatch_group<8, true>(group, p, num_seqs, st)
+                     : dispatch_group<8, false>(group, p, num_seqs, st);
+    return fused ? dispatch_group<16, true>(group, p, num_seqs, st)
+                 : dispatch_group<16, false>(group, p, num_seqs, st);
 }
 
 }  // namespace
@@ -622,8 +660,7 @@ int decode_entry(const void *q, const void *k_cache, const void *v_cache, const 
         p.part_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kCounterBytes);
         p.part_ml = p.part_o + (size_t)num_seqs * p.max_splits * num_q_heads * kD;
     }
-    const size_t smem = (size_t)kStages * 2 * kT * num_kv_heads * kD * 2 + 2 * kStages * 8 + kStages * 4 + 16;
-    return dispatch(group, p, num_seqs, smem, (cudaStream_t)stream);
+    return dispatch(group, p, num_seqs, (cudaStream_t)stream);
 }
 
 }  // namespace
@@ -768,6 +805,5 @@ extern "C" int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, 
         p.part_o = static_cast<float *>(scratch);
         p.part_ml = p.part_o + (size_t)num_seqs * p.max_splits * num_q_heads * kD;
     }
-    const size_t smem = (size_t)kStages * 2 * kT * num_kv_heads * kD * 2 + 2 * kStages * 8 + kStages * 4 + 16;
-    return dispatch(group, p, num_seqs, smem, (cudaStream_t)stream);
+    return dispatch(group, p, num_seqs, (cudaStream_t)stream);
 }
