@@ -46,6 +46,9 @@ CASES = [
     ("g8-bs32", [10, 31, 32, 33, 900], 16, 2, 32, 1),
     ("g4-hkv1", [5, 130, 1025], 4, 1, 128, 0),
     ("g2-hkv16", [2, 40, 513], 32, 16, 16, 0),
+    ("g8-hkv8", [1, 9, 255, 256, 1100, 3000], 64, 8, 256, 1),   # two consumer warps per kv head
+    ("g8-hkv16", [3, 500, 1300], 128, 16, 16, 0),
+    ("g4-hkv12", [5, 300, 2100], 48, 12, 128, 1),
 ]
 
 

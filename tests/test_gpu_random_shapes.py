@@ -1,4 +1,4 @@
-"""Seeded random shapes for decode and prefill against the oracle: group sizes 1-8, every supported
+"""Seeded random shapes for decode and prefill against the oracle: group sizes 1-8 (kv heads 1-16), every supported
 block size, lengths drawn around block and tile edges (1, bs-1, bs, bs+1, 127, 128, 129, ...), padding
 rows, and pools whose unused tails hold NaN patterns.  Small enough that the oracle runs every row."""
 import numpy as np
@@ -10,7 +10,7 @@ from tests.gpu_util import DeviceBatch, compare, host_f32, oracle_cache_after_st
 
 pytestmark = pytest.mark.gpu
 
-GROUPS = [(8, 8), (16, 8), (32, 8), (16, 2), (8, 1), (32, 16)]
+GROUPS = [(8, 8), (16, 8), (32, 8), (16, 2), (8, 1), (32, 16), (64, 8), (48, 12)]
 BLOCKS = [16, 32, 64, 128, 256]
 
 
