@@ -8,15 +8,16 @@
 // base^(-2j/D); rotation in fp32, cast to bf16); q goes to q_out for attention, and the roped k
 // and the untouched v are stored at the token's slot (slot -1 stores nothing).
 //
-// How (GB300): a memory-bound elementwise pass with a per-head reduction.  One warp handles one
-// token: lane l owns frequencies 2l and 2l+1, so the token's sines and cosines are computed once
-// and shared by all its heads.  For each head vector of 128 values lane l holds dims 2l, 2l+1 and
-// their rotation partners 64+2l, 64+2l+1, so the rotation needs no shuffles and every load and
-// store is a coalesced 128-byte row half; the sum of squares is a 5-level butterfly.  The loads
-// of kItems heads go out together before any arithmetic, to keep enough bytes in flight for HBM.
-// The two bf16 roundings work on pairs: one conversion rounds two normalised values, and one
-// bf16x2 multiply forms both weight products (the kernel is issue-bound, so instruction count
-// matters).
+// How (GB300): a memory-bound elementwise pass with a per-head reduction, issue-bound on its
+// arithmetic, so the layout is chosen for few instructions per value.  One warp handles one token
+// and four of its heads at a time: 8 lanes per head, lane i of a head holding dims 8i..8i+7 and
+// their rotation partners 64+8i..64+8i+7 (two 16-byte loads, two 16-byte stores), so the rotation
+// needs no shuffles and the sum of squares is a 3-level butterfly inside the 8 lanes.  The token's
+// sines and cosines are computed once, two frequencies per lane, and gathered to the lanes that
+// use them with shuffles.  Values are held as fp32 pairs and the arithmetic uses the packed pair
+// instructions (squares, the scaling by 1/rms and the rotation); the two bf16 roundings also work
+// on pairs (one conversion rounds two normalised values, one bf16x2 multiply forms both weight
+// products).  The loads of kBatch groups of four heads go out together before any arithmetic.
 // The RoPE frequencies are computed once per call on the host (64 floats, passed as a kernel
 // parameter); the angle product and sincosf are fp32, as the pages compute them.
 #include <cmath>
@@ -28,8 +29,10 @@ namespace {
 using namespace nvkv;
 
 constexpr int kD = 128;
-constexpr int kItems = 8;              // head vectors of a token whose loads go out together
-constexpr int kWarps = 8;              // per block
+constexpr int kGroup = 4;              // heads per warp instruction (8 lanes each)
+constexpr int kBatch = 4;              // groups of four heads whose loads go out together
+constexpr int kWarps = 4;              // per block
+constexpr int kBlocksPerSm = 4;        // 116 registers a thread: four 128-thread blocks per SM
 
 struct RopeParams {
     const __nv_bfloat16 *qkv;
@@ -64,79 +67,130 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
     return d;
 }
 
-__global__ void __launch_bounds__(kWarps * 32) qk_norm_rope_store_kernel(const __grid_constant__ RopeParams p)
+__device__ __forceinline__ uint32_t word(const uint4 &v, int m)
+{
+    return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
+}
+
+// RMSNorm (fp32 statistics; normalised value cast to bf16, times the bf16 weight) of 8 values
+// held as 4 bf16 pairs, given 1/rms: returns the 4 fp32 pairs of the bf16 results.
+__device__ __forceinline__ void norm8(const float2 (&x)[4], float r, const uint4 &w, float2 (&n)[4])
+{
+    const float2 r2 = make_float2(r, r);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const float2 xr = __fmul2_rn(x[m], r2);
+        n[m] = bf16x2_to_f2(mul_bf16x2(pack_bf16x2(xr.x, xr.y), word(w, m)));
+    }
+}
+
+__global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm)
+    qk_norm_rope_store_kernel(const __grid_constant__ RopeParams p)
 {
     const int lane = threadIdx.x & 31;
+    const int gi = lane >> 3;              // head of a group of four
+    const int li = lane & 7;               // dims 8li..8li+7 and 64+8li..64+8li+7
     const int heads = p.num_q_heads + 2 * p.num_kv_heads;
     const int qk_heads = p.num_q_heads + p.num_kv_heads;
     const int64_t dkv = (int64_t)p.num_kv_heads * kD;
     const int64_t warp_id = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * kWarps;
-    // this lane's weights (dims 2l, 2l+1 and 64+2l, 64+2l+1) and frequencies (2l, 2l+1)
-    const uint32_t qw1 = __ldg(reinterpret_cast<const uint32_t *>(p.q_weight) + lane);
-    const uint32_t qw2 = __ldg(reinterpret_cast<const uint32_t *>(p.q_weight) + 32 + lane);
-    const uint32_t kw1 = __ldg(reinterpret_cast<const uint32_t *>(p.k_weight) + lane);
-    const uint32_t kw2 = __ldg(reinterpret_cast<const uint32_t *>(p.k_weight) + 32 + lane);
+    // this lane's weights (4-byte loads: the weights need only 4-byte alignment)
+    const uint32_t *qwp = reinterpret_cast<const uint32_t *>(p.q_weight);
+    const uint32_t *kwp = reinterpret_cast<const uint32_t *>(p.k_weight);
+    const uint4 qw1 = make_uint4(__ldg(qwp + 4 * li), __ldg(qwp + 4 * li + 1), __ldg(qwp + 4 * li + 2),
+                                 __ldg(qwp + 4 * li + 3));
+    const uint4 qw2 = make_uint4(__ldg(qwp + 32 + 4 * li), __ldg(qwp + 33 + 4 * li), __ldg(qwp + 34 + 4 * li),
+                                 __ldg(qwp + 35 + 4 * li));
+    const uint4 kw1 = make_uint4(__ldg(kwp + 4 * li), __ldg(kwp + 4 * li + 1), __ldg(kwp + 4 * li + 2),
+                                 __ldg(kwp + 4 * li + 3));
+    const uint4 kw2 = make_uint4(__ldg(kwp + 32 + 4 * li), __ldg(kwp + 33 + 4 * li), __ldg(kwp + 34 + 4 * li),
+                                 __ldg(kwp + 35 + 4 * li));
+    // lane l computes the angles of frequencies 2l and 2l+1
     const float f0 = p.inv_freq[2 * lane], f1 = p.inv_freq[2 * lane + 1];
 
-    // one warp per token: the token's angles are shared by all its heads
     for (int64_t t = warp_id; t < p.n_tokens; t += nwarps) {
-        const uint32_t *row = reinterpret_cast<const uint32_t *>(p.qkv + t * p.row_stride);
+        const uint4 *row = reinterpret_cast<const uint4 *>(p.qkv + t * p.row_stride);
         const float pos = (float)__ldg(p.positions + t);
         float s0, c0, s1, c1;
         sincosf(pos * f0, &s0, &c0);
         sincosf(pos * f1, &s1, &c1);
+        // pair m of this lane (dims 8li+2m, 8li+2m+1) rotates at frequencies 8li+2m, 8li+2m+1,
+        // computed by lane 4li+m
+        float2 cs[4], sn[4], nsn[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int src = 4 * li + m;
+            cs[m] = make_float2(__shfl_sync(0xffffffffu, c0, src), __shfl_sync(0xffffffffu, c1, src));
+            sn[m] = make_float2(__shfl_sync(0xffffffffu, s0, src), __shfl_sync(0xffffffffu, s1, src));
+            nsn[m] = make_float2(-sn[m].x, -sn[m].y);
+        }
         const int sraw = __ldg(p.slot_mapping + t);
         const bool store = sraw >= 0 && sraw < p.num_slots;
         if (lane == 0 && (sraw < -1 || sraw >= p.num_slots))
             flag_error(p.d_err, NV_DERR_SLOT_RANGE);
         const int64_t slot = store ? sraw : 0;
-        // the token's heads, kItems at a time: all loads first, then the arithmetic
-        for (int h0 = 0; h0 < heads; h0 += kItems) {
-            uint32_t a[kItems], b[kItems];
+        for (int h0 = 0; h0 < heads; h0 += kGroup * kBatch) {
+            uint4 a[kBatch], b[kBatch];
 #pragma unroll
-            for (int i = 0; i < kItems; ++i) {
-                const int h = h0 + i;
-                a[i] = b[i] = 0;
+            for (int i = 0; i < kBatch; ++i) {
+                const int h = h0 + kGroup * i + gi;
+                a[i] = b[i] = make_uint4(0, 0, 0, 0);
                 if (h < heads && (h < p.num_q_heads || store)) {
-                    a[i] = __ldg(row + h * (kD / 2) + lane);          // dims 2l, 2l+1
-                    b[i] = __ldg(row + h * (kD / 2) + 32 + lane);     // dims 64+2l, 64+2l+1
+                    a[i] = __ldg(row + h * (kD / 8) + li);          // dims 8li .. 8li+7
+                    b[i] = __ldg(row + h * (kD / 8) + 8 + li);      // dims 64+8li .. 64+8li+7
                 }
             }
 #pragma unroll
-            for (int i = 0; i < kItems; ++i) {
-                const int h = h0 + i;
-                if (h >= heads)
-                    break;
-                const bool is_q = h < p.num_q_heads;
-                if (!is_q && !store)
-                    continue;
-                if (h >= qk_heads) {                   // v: stored unchanged
-                    uint32_t *dst = reinterpret_cast<uint32_t *>(p.v_cache + slot * dkv + (int64_t)(h - qk_heads) * kD);
-                    dst[lane] = a[i];
-                    dst[32 + lane] = b[i];
-                    continue;
-                }
-                // RMSNorm over the head's 128 values (fp32 statistics)
-                const float2 x1 = bf16x2_to_f2(a[i]), x2 = bf16x2_to_f2(b[i]);
-                float ss = x1.x * x1.x + x1.y * x1.y + x2.x * x2.x + x2.y * x2.y;
+            for (int i = 0; i < kBatch; ++i) {
+                if (h0 + kGroup * i >= heads)
+                    break;                                          // the same for every lane
+                const int h = h0 + kGroup * i + gi;
+                float2 xa[4], xb[4];
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    ss += __shfl_xor_sync(0xffffffffu, ss, o);
-                const float r = rsqrtf(ss * (1.0f / kD) + p.eps);
-                const uint32_t w1 = is_q ? qw1 : kw1, w2 = is_q ? qw2 : kw2;
-                // cast to bf16 (two values per conversion), then the bf16 product with the weight
-                const float2 na = bf16x2_to_f2(mul_bf16x2(pack_bf16x2(x1.x * r, x1.y * r), w1));
-                const float2 nb = bf16x2_to_f2(mul_bf16x2(pack_bf16x2(x2.x * r, x2.y * r), w2));
-                const float n0 = na.x, n1 = na.y, n2 = nb.x, n3 = nb.y;
-                // RoPE, rotate-half: (n0, n2) at frequency 2l, (n1, n3) at frequency 2l+1
-                const uint32_t y1 = pack_bf16x2(n0 * c0 - n2 * s0, n1 * c1 - n3 * s1);
-                const uint32_t y2 = pack_bf16x2(n2 * c0 + n0 * s0, n3 * c1 + n1 * s1);
-                uint32_t *dst = is_q
-                    ? reinterpret_cast<uint32_t *>(p.q_out + (t * p.num_q_heads + h) * kD)
-                    : reinterpret_cast<uint32_t *>(p.k_cache + slot * dkv + (int64_t)(h - p.num_q_heads) * kD);
-                dst[lane] = y1;
-                dst[32 + lane] = y2;
+                for (int m = 0; m < 4; ++m) {
+                    xa[m] = bf16x2_to_f2(word(a[i], m));
+                    xb[m] = bf16x2_to_f2(word(b[i], m));
+                }
+                // sum of squares over the head's 128 values: 16 here, then the 8 lanes
+                float2 q2 = __fmul2_rn(xa[0], xa[0]);
+#pragma unroll
+                for (int m = 1; m < 4; ++m)
+                    q2 = __ffma2_rn(xa[m], xa[m], q2);
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    q2 = __ffma2_rn(xb[m], xb[m], q2);
+                float ss = q2.x + q2.y;
+                ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (h >= heads || (h >= p.num_q_heads && !store)) {
+                    // no head here, or a k / v row of a token that stores nothing
+                } else if (h >= qk_heads) {                         // v: stored unchanged
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.v_cache + slot * dkv + (int64_t)(h - qk_heads) * kD);
+                    dst[li] = a[i];
+                    dst[8 + li] = b[i];
+                } else {
+                    const bool is_q = h < p.num_q_heads;
+                    const float r = rsqrtf(ss * (1.0f / kD) + p.eps);
+                    float2 na[4], nb[4];
+                    norm8(xa, r, is_q ? qw1 : kw1, na);
+                    norm8(xb, r, is_q ? qw2 : kw2, nb);
+                    // RoPE, rotate-half: y_j = n_j cos - n_{j+64} sin, y_{j+64} = n_{j+64} cos + n_j sin
+                    uint32_t y1[4], y2[4];
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const float2 u = __ffma2_rn(nb[m], nsn[m], __fmul2_rn(na[m], cs[m]));
+                        const float2 v = __ffma2_rn(na[m], sn[m], __fmul2_rn(nb[m], cs[m]));
+                        y1[m] = pack_bf16x2(u.x, u.y);
+                        y2[m] = pack_bf16x2(v.x, v.y);
+                    }
+                    uint4 *dst = is_q
+                        ? reinterpret_cast<uint4 *>(p.q_out + (t * p.num_q_heads + h) * kD)
+                        : reinterpret_cast<uint4 *>(p.k_cache + slot * dkv + (int64_t)(h - p.num_q_heads) * kD);
+                    dst[li] = make_uint4(y1[0], y1[1], y1[2], y1[3]);
+                    dst[8 + li] = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+                }
             }
         }
     }
@@ -193,7 +247,7 @@ extern "C" int nv_qk_norm_rope_store(const void *qkv, int64_t qkv_row_stride, co
         p.inv_freq[j] = 1.0f / powf(rope_theta, (float)(2 * j) / (float)kD);
 
     const int64_t blocks_needed = ((int64_t)n_tokens + kWarps - 1) / kWarps;
-    const int64_t cap = (int64_t)sms * 4;      // half the resident limit: measured a little faster
+    const int64_t cap = (int64_t)sms * kBlocksPerSm;   // one resident wave
     const int grid = (int)(blocks_needed < cap ? blocks_needed : cap);
     qk_norm_rope_store_kernel<<<grid, kWarps * 32, 0, (cudaStream_t)stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
