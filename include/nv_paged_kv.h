@@ -62,7 +62,7 @@ typedef enum nv_status {
 #define NV_DERR_TIMEOUT 0x8       /* a bounded wait on an asynchronous copy gave up */
 #define NV_DERR_SLOT_MISMATCH 0x10 /* fused store + decode: a slot that is not position L-1's (row not stored) */
 #define NV_DERR_VALUE 0x20         /* sampler: a temperature that is not positive and finite (token -1);
-                                      decode: a split counter of the workspace was not zero */
+                                      decode and sampler: a counter of the workspace was not zero */
 
 /* Human-readable name of an nv_status value (static string). */
 const char *nv_status_string(int status);
@@ -167,10 +167,16 @@ int nv_prepare_prefill(const int32_t *num_cached, const int32_t *num_scheduled, 
  *                 NV_DERR_VALUE is set).
  *   draws         float32 [num_rows, draws_stride] (stride a multiple of 4).  Both bases 16-byte aligned.
  *   tokens        int64 [num_rows] (out).
- *   workspace     at least nv_sample_workspace_size(num_rows, vocab) bytes, 16-byte aligned.
+ *   workspace     at least nv_sample_workspace_size(num_rows, vocab) bytes, 16-byte aligned, ZERO-FILLED
+ *                 before its first use.  Its first 256 KiB hold one counter per row, which every call
+ *                 leaves at zero again, so one workspace, zeroed once, serves any later call (any batch
+ *                 size); the rest is scratch.  Calls that share a workspace must not run concurrently.
+ *                 A counter found non-zero (a workspace that was not zero-filled) sets NV_DERR_VALUE
+ *                 and leaves that row's token unspecified.
  * The argmax is taken over logits_i * log2(e) / T - log2(max(E_i, 1e-10)), which orders the
  * entries exactly as p_i / E_i does; rounding can only matter between entries within a few
- * float32 ulps of each other.  Two launches.
+ * float32 ulps of each other.  One launch: a row is split over several CTAs and the row's last
+ * CTA to finish writes its token.
  */
 size_t nv_sample_workspace_size(int32_t num_rows, int32_t vocab);
 

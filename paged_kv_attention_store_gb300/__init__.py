@@ -143,8 +143,8 @@ def nv_sample_exponential_race(logits, temperatures, draws, tokens=None, workspa
     _need(tuple(draws.shape) == (B, V) and int(temperatures.shape[0]) == B, "one temperature and V draws per row")
     if tokens is None:
         tokens = torch.empty(B, dtype=torch.int64, device=logits.device)
-    if workspace is None:
-        workspace = torch.empty(max(int(load_library().nv_sample_workspace_size(B, V)), 16), dtype=torch.uint8,
+    if workspace is None:   # zero-filled: its per-row counters must start at zero (the calls leave them so)
+        workspace = torch.zeros(max(int(load_library().nv_sample_workspace_size(B, V)), 16), dtype=torch.uint8,
                                 device=logits.device)
     rc = load_library().nv_sample_exponential_race(_ptr(logits), logits.stride(0), _ptr(temperatures), _ptr(draws),
                                                    draws.stride(0), B, V, _ptr(tokens), _ptr(workspace),

@@ -10,8 +10,9 @@
 // logits + 4 bytes of draw per vocabulary entry).  Computed in base 2 (scores scaled by log2 e, the
 // draw's log2 from the special-function unit).  A row is split over a few CTAs; each thread keeps
 // its best (score, index), a block reduces them as 64-bit keys (order-preserving score bits above,
-// the complement of the index below, so equal scores prefer the smaller index), and a small merge
-// kernel takes the best key per row.
+// the complement of the index below, so equal scores prefer the smaller index) and writes the
+// block's best key; the row's last CTA to finish (a per-row counter in the workspace) takes the best
+// of the row's keys and writes the token, so no separate merge pass runs.
 #include "nv_common.cuh"
 
 namespace {
@@ -19,12 +20,18 @@ namespace {
 using namespace nvkv;
 
 constexpr int kThreads = 256;
+constexpr int kUnroll = 4;         // vectors per thread whose loads go out together (1: 79.8 us, 8: 75.7)
+// Per-row counters sit at the start of the workspace in a region of fixed size, so a workspace reused
+// for batches of different sizes keeps them in place (they are zero between calls).
+constexpr int kMaxRows = 65536;
+constexpr size_t kCounterBytes = (size_t)kMaxRows * sizeof(int32_t);
 
 struct SampleParams {
     const __nv_bfloat16 *logits;
     const float *draws;
     const float *temperatures;
     unsigned long long *partial;    // [num_rows, chunks]
+    int32_t *done;                  // [num_rows]: chunks finished in this call; zero between calls
     int64_t *tokens;
     int32_t *d_err;
     int64_t logits_stride;          // elements
@@ -72,13 +79,11 @@ __global__ void __launch_bounds__(kThreads) sample_partial_kernel(const SamplePa
         const float *er = p.draws + (int64_t)row * p.draws_stride;
         float bs = -INFINITY;
         int bi = lo;
-        // 8 entries per thread per step: 16 bytes of logits, 32 bytes of draws
+        // 8 entries per vector: 16 bytes of logits, 32 bytes of draws.  A thread takes vectors
+        // v, v + kThreads, ... in increasing order, kUnroll of them loaded before any is compared, so
+        // more bytes are in flight; comparing them in order keeps the first index on ties.
         const int nvec = (hi - lo) / 8;
-        for (int v = threadIdx.x; v < nvec; v += kThreads) {
-            const int i0 = lo + v * 8;
-            const uint4 lq = ld_stream_u4(lr + i0);
-            const float4 e0 = __ldcs(reinterpret_cast<const float4 *>(er + i0));
-            const float4 e1 = __ldcs(reinterpret_cast<const float4 *>(er + i0) + 1);
+        auto take = [&](int i0, const uint4 &lq, const float4 &e0, const float4 &e1) {
             const float l[8] = {bf16lo(lq.x), bf16hi(lq.x), bf16lo(lq.y), bf16hi(lq.y),
                                 bf16lo(lq.z), bf16hi(lq.z), bf16lo(lq.w), bf16hi(lq.w)};
             const float e[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
@@ -90,6 +95,26 @@ __global__ void __launch_bounds__(kThreads) sample_partial_kernel(const SamplePa
                     bi = i0 + j;
                 }
             }
+        };
+        int v = threadIdx.x;
+        for (; v + (kUnroll - 1) * kThreads < nvec; v += kUnroll * kThreads) {
+            uint4 lq[kUnroll];
+            float4 e0[kUnroll], e1[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int i0 = lo + (v + u * kThreads) * 8;
+                lq[u] = ld_stream_u4(lr + i0);
+                e0[u] = __ldcs(reinterpret_cast<const float4 *>(er + i0));
+                e1[u] = __ldcs(reinterpret_cast<const float4 *>(er + i0) + 1);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u)
+                take(lo + (v + u * kThreads) * 8, lq[u], e0[u], e1[u]);
+        }
+        for (; v < nvec; v += kThreads) {
+            const int i0 = lo + v * 8;
+            take(i0, ld_stream_u4(lr + i0), __ldcs(reinterpret_cast<const float4 *>(er + i0)),
+                 __ldcs(reinterpret_cast<const float4 *>(er + i0) + 1));
         }
         for (int i = lo + nvec * 8 + threadIdx.x; i < hi; i += kThreads) {   // ragged tail
             const float s = race_score(__bfloat162float(lr[i]), er[i], scale2);
@@ -118,29 +143,37 @@ __global__ void __launch_bounds__(kThreads) sample_partial_kernel(const SamplePa
             const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
             best = other > best ? other : best;
         }
-        if (threadIdx.x == 0)
+        // Publish the block's key, then count the chunk as done; the row's last chunk to get here
+        // reads every key of the row (from L2, past this SM's L1) and writes the token.  The fence
+        // before the count makes the key visible device-wide first; on the last chunk, the fence
+        // after it orders the reads after every other chunk's key.
+        int last = 0;
+        if (threadIdx.x == 0) {
             p.partial[(int64_t)row * p.chunks + chunk] = best;
-    }
-}
-
-__global__ void __launch_bounds__(128) sample_merge_kernel(const SampleParams p)
-{
-    const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= p.num_rows)
-        return;
-    unsigned long long best = 0ull;
-    for (int c = lane; c < p.chunks; c += 32) {
-        const unsigned long long k = p.partial[(int64_t)row * p.chunks + c];
-        best = k > best ? k : best;
-    }
+            __threadfence();
+            const int prev = atomicAdd(p.done + row, 1);
+            if (prev < 0 || prev >= p.chunks)
+                flag_error(p.d_err, NV_DERR_VALUE);   // the counters were not zero: workspace not zero-filled
+            last = prev == p.chunks - 1;
+            __threadfence();
+        }
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+            unsigned long long m = 0ull;
+            for (int c = threadIdx.x; c < p.chunks; c += 32) {
+                const unsigned long long k = __ldcg(p.partial + (int64_t)row * p.chunks + c);
+                m = k > m ? k : m;
+            }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-        best = other > best ? other : best;
+            for (int o = 16; o > 0; o >>= 1) {
+                const unsigned long long other = __shfl_xor_sync(0xffffffffu, m, o);
+                m = other > m ? other : m;
+            }
+            if (threadIdx.x == 0) {
+                p.tokens[row] = m == 0ull ? -1 : (int64_t)(0xFFFFFFFFu - (uint32_t)(m & 0xFFFFFFFFull));
+                p.done[row] = 0;      // ready for the next call
+            }
+        }
     }
-    if (lane == 0)
-        p.tokens[row] = best == 0ull ? -1 : (int64_t)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
 }
 
 int sample_chunks(int32_t num_rows, int32_t vocab)
@@ -157,7 +190,7 @@ extern "C" size_t nv_sample_workspace_size(int32_t num_rows, int32_t vocab)
 {
     if (num_rows <= 0 || vocab <= 0)
         return 0;
-    return (size_t)num_rows * sample_chunks(num_rows, vocab) * sizeof(unsigned long long);
+    return kCounterBytes + (size_t)num_rows * sample_chunks(num_rows, vocab) * sizeof(unsigned long long);
 }
 
 extern "C" int nv_sample_exponential_race(const void *logits, int64_t logits_stride, const float *temperatures,
@@ -183,7 +216,8 @@ extern "C" int nv_sample_exponential_race(const void *logits, int64_t logits_str
     p.logits = static_cast<const __nv_bfloat16 *>(logits);
     p.draws = draws;
     p.temperatures = temperatures;
-    p.partial = static_cast<unsigned long long *>(workspace);
+    p.done = static_cast<int32_t *>(workspace);
+    p.partial = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) + kCounterBytes);
     p.tokens = tokens;
     p.d_err = d_err;
     p.logits_stride = logits_stride;
@@ -193,8 +227,5 @@ extern "C" int nv_sample_exponential_race(const void *logits, int64_t logits_str
     p.chunks = chunks;
     p.chunk_len = (((vocab + chunks - 1) / chunks) + 7) / 8 * 8;
     sample_partial_kernel<<<dim3(chunks, num_rows), kThreads, 0, (cudaStream_t)stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess)
-        return NV_ERR_CUDA;
-    sample_merge_kernel<<<(num_rows + 3) / 4, 128, 0, (cudaStream_t)stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }

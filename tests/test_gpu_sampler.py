@@ -87,3 +87,34 @@ def test_sampler_bad_temperature_is_flagged():
     assert err & nv.NV_DERR_VALUE and got[2] == -1
     want = oracle.default().sample(logits[[0, 1, 3]], temps[[0, 1, 3]], draws[[0, 1, 3]])
     assert np.array_equal(got[[0, 1, 3]], want)
+
+
+def test_sampler_workspace_reused_across_batch_sizes():
+    """One zero-filled workspace serves calls of different row counts and vocabularies: the per-row
+    counters the last block of a row uses are left at zero by every call."""
+    import torch
+    ws = torch.zeros(max(nv.load_library().nv_sample_workspace_size(B, V) for B, V in ((300, 4096), (7, 50000))),
+                     dtype=torch.uint8, device="cuda")
+    orc = oracle.default()
+    for B, V, seed in ((300, 4096, 1), (7, 50000, 2), (300, 4096, 3), (7, 50000, 4)):
+        logits, temps, draws = _inputs(B, V, seed)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        tok = nv.nv_sample_exponential_race(dev_bf16(logits), torch.from_numpy(temps).cuda(),
+                                            torch.from_numpy(draws).cuda(), workspace=ws, d_err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        want = orc.sample(logits, temps, draws, threads=8)
+        assert (tok.cpu().numpy() != want).sum() <= max(1, B // 100)
+
+
+def test_sampler_workspace_not_zero_filled_is_flagged():
+    """Row counters that do not start at zero (a workspace that was not zero-filled) are reported."""
+    import torch
+    logits, temps, draws = _inputs(16, 50000, 6)
+    ws = torch.full((nv.load_library().nv_sample_workspace_size(16, 50000),), 0xFF, dtype=torch.uint8,
+                    device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nv.nv_sample_exponential_race(dev_bf16(logits), torch.from_numpy(temps).cuda(), torch.from_numpy(draws).cuda(),
+                                  workspace=ws, d_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & nv.NV_DERR_VALUE
