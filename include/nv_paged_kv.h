@@ -57,7 +57,9 @@ typedef enum nv_status {
 
 /* Bits OR-ed into *d_err by the kernels. */
 #define NV_DERR_SLOT_RANGE 0x1    /* slot_mapping entry < -1 or >= num_slots: row skipped */
-#define NV_DERR_BLOCK_RANGE 0x2   /* a needed block-table entry outside [0, num_blocks): its keys skipped */
+#define NV_DERR_BLOCK_RANGE 0x2   /* a needed block-table entry outside [0, num_blocks): nothing is read
+                                     from it; that sequence's output is not meaningful (the store and
+                                     the split-KV decode of groups 1-4 skip its keys) */
 #define NV_DERR_LENGTH 0x4        /* a length exceeds the block table, the host hint, or is negative */
 #define NV_DERR_TIMEOUT 0x8       /* a bounded wait on an asynchronous copy gave up */
 #define NV_DERR_SLOT_MISMATCH 0x10 /* fused store + decode: a slot that is not position L-1's (row not stored) */
@@ -185,8 +187,10 @@ int nv_sample_exponential_race(const void *logits, int64_t logits_stride, const 
                                size_t workspace_bytes, int32_t *d_err, nv_stream_t stream);
 
 /*
- * Bytes of workspace nv_paged_decode_attn needs for this batch (0 means none).  Depends only
- * on its arguments, so it can be sized once for the largest batch and reused.
+ * Bytes of workspace nv_paged_decode_attn needs for this batch: 256 KiB of split counters, then the
+ * larger of the split-KV partials (groups 1-4; none when one split covers max_context_len) and the
+ * tile kernel's work list (groups 8 and 16: 64 bytes + 32 per sequence).  Depends only on its
+ * arguments, so it can be sized once for the largest batch and reused.
  */
 size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                       int32_t max_context_len);
@@ -202,6 +206,13 @@ size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
  * block_size + j % block_size.  fp32 accumulation and softmax, bf16 output rounded once.
  * A row with L == 0 (graph padding) gets zeros.
  *
+ * Groups (num_q_heads / num_kv_heads) 1, 2, 4: a split-KV flash-decoding kernel on CUDA cores (one
+ * launch).  Groups 8 and 16: each query head of a group multiplies every KV byte, and the CUDA-core
+ * kernel's FMAs no longer keep up with HBM (measured 0.54 of the roofline at group 8), so the call
+ * runs the tcgen05 tile kernel of nv_paged_prefill_attn with one query row per sequence at position
+ * L-1 (two launches: a work-list pre-pass, which also zeroes the rows with L == 0, and the tile
+ * kernel).  The two paths round differently (both within the parity bar of the fp32 definition).
+ *
  *   q, out        bf16 [num_seqs, num_q_heads, head_dim], contiguous, 16-byte aligned.
  *   block_tables  int32 [num_seqs, bt_stride]; context_lens int32 [num_seqs].
  *   num_blocks    pool size in blocks (block ids must lie in [0, num_blocks)).
@@ -209,8 +220,8 @@ size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
  *                 grid without reading device memory).  A sequence longer than it is
  *                 truncated to it and flagged NV_DERR_LENGTH.  <= bt_stride*block_size.
  *   scale         softmax scale (head_dim ** -0.5 in the pages).
- *   workspace     device scratch of at least nv_paged_decode_workspace_size(...) bytes
- *                 (may be NULL when that size is 0), 16-byte aligned.  Its first 256 KiB hold
+ *   workspace     device scratch of at least nv_paged_decode_workspace_size(...) bytes, 16-byte
+ *                 aligned (groups 1-4 may pass NULL when one split covers max_context_len).  Its first 256 KiB hold
  *                 the per-sequence split counters: they must be ZERO before the first call
  *                 that uses the workspace (allocate it zero-filled), and every call leaves them
  *                 zero, whatever the batch; the rest needs no initialisation.  A counter found
@@ -247,7 +258,8 @@ int nv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache
  *                 not written, position L-1 is read from the pool, and NV_DERR_SLOT_MISMATCH is set
  *                 (NV_DERR_SLOT_RANGE when it lies outside the pool).
  * The result (cache and out) equals nv_store_kvcache then nv_paged_decode_attn with the same
- * arguments whenever the slots follow that rule.  The new slots must not lie in another
+ * arguments whenever the slots follow that rule.  Groups 8 and 16 (which decode on the tile kernel)
+ * apply the same rule in a separate store pass before the decode's two launches.  The new slots must not lie in another
  * sequence's history within the same call (they never do: a new token's slot belongs to its
  * own sequence).
  */
@@ -268,7 +280,8 @@ int nv_store_decode_attn(const void *q, const void *k, int64_t k_row_stride, con
  * partials live in a fixed device array of NV_DECODE_STATIC_SCRATCH_BYTES inside the library,
  * which every GPU that loads the library holds until the process exits.
  *
- * Arguments and results are those of nv_paged_decode_attn (same kernels).  The split length
+ * Arguments and results are those of nv_paged_decode_attn (same kernels; groups 8 and 16 keep the
+ * tile kernel's work list in the same static array).  The split length
  * is the usual one, doubled (up to 4096 positions) while the partials would not fit the
  * array; a batch whose partials still exceed it (num_seqs * splits * num_q_heads * 520 bytes)
  * is rejected with NV_ERR_WORKSPACE before anything is enqueued.

@@ -13,9 +13,10 @@
 //     memory, completing on an mbarrier.  A producer warp keeps three such chunks in
 //     flight per CTA (two CTAs per SM), reading one block-table entry per block.
 //   * Consumer warp w owns kv head w and its G = Hq/Hkv query heads, so every K/V element
-//     is read from shared memory once and used G times (GQA sharing).  At G = 8 two warps
-//     share a kv head, four query heads each, and the CTA (one per SM) keeps six chunks in
-//     flight.  A half-warp handles
+//     is read from shared memory once and used G times (GQA sharing).  This kernel takes
+//     G = 1, 2, 4; with G = 8 or 16 the warps would do too many FMAs per KV byte to keep up
+//     with HBM, and decode runs on the tcgen05 tile kernel instead (tile_attention.cuh), as a
+//     prefill of one query row per sequence.  A half-warp handles
 //     one position at a time, each lane 8 of the 128 dims; partial dot products are reduced
 //     with a reduce-scatter over 4 shuffle levels that leaves each lane the full score of
 //     one of the G heads, so the exponential is computed once per (position, head).
@@ -33,6 +34,7 @@
 #include <mutex>
 
 #include "nv_common.cuh"
+#include "tile_attention.cuh"
 
 namespace {
 
@@ -148,35 +150,18 @@ __device__ __forceinline__ void merge_splits(const DecodeParams &p, int b, int n
     }
 }
 
-// Consumer warps per kv head: with 8 query heads per kv head, two warps split them (4 each) and
-// share every staged K/V element, so a warp's per-position work stays that of a group of 4 (one
-// warp holding all 8 measured 2.75x slower: its FMA work doubled and its registers spilled).
-__host__ __device__ constexpr int decode_warps_per_kv_head(int group, int max_kv_heads)
-{
-    return (group == 8 && max_kv_heads <= 8) ? 2 : 1;
-}
-
-// Chunks in flight per CTA.  Three stages of 8 kv heads take 96 KB, so two CTAs share an SM; a
-// CTA with two warps per kv head has too many registers for a second CTA on its SM, so it keeps
-// six stages (192 KB) in flight by itself.
-__host__ __device__ constexpr int decode_stages(int group, int max_kv_heads)
-{
-    return decode_warps_per_kv_head(group, max_kv_heads) == 2 ? 6 : 3;
-}
+constexpr int kStages = 3;   // chunks in flight per CTA: 96 KB at 8 kv heads, two CTAs per SM
 
 __host__ __device__ constexpr size_t decode_smem_bytes(int stages, int num_kv_heads)
 {
     return (size_t)stages * 2 * kT * num_kv_heads * kD * 2 + 2 * stages * 8 + stages * 4 + 16;
 }
 
-template <int GQ, int MAX_KV_HEADS, bool kFused>
-__global__ void __launch_bounds__((MAX_KV_HEADS * decode_warps_per_kv_head(GQ, MAX_KV_HEADS) + 1) * 32,
-                                  (MAX_KV_HEADS <= 8 && decode_warps_per_kv_head(GQ, MAX_KV_HEADS) == 1 ? 2 : 1))
+template <int G, int MAX_KV_HEADS, bool kFused>
+__global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, MAX_KV_HEADS <= 8 ? 2 : 1)
     paged_decode_kernel(const DecodeParams p)
 {
-    constexpr int kWPH = decode_warps_per_kv_head(GQ, MAX_KV_HEADS);   // consumer warps per kv head
-    constexpr int G = GQ / kWPH;                                        // query heads per consumer warp
-    constexpr int kS = decode_stages(GQ, MAX_KV_HEADS);                 // chunks in flight
+    constexpr int kS = kStages;
     extern __shared__ __align__(128) uint8_t smem[];
     const int hkv = p.num_kv_heads;
     const int dkv = hkv * kD;                        // elements per pool row
@@ -242,7 +227,7 @@ __global__ void __launch_bounds__((MAX_KV_HEADS * decode_warps_per_kv_head(GQ, M
     if (threadIdx.x == 0) {
         for (int s = 0; s < kS; ++s) {
             mbar_init(bar_base + 8 * s, 1);                    // full: producer arrive + tx bytes
-            mbar_init(bar_base + 8 * (kS + s), hkv * kWPH);   // empty: one arrive per consumer warp
+            mbar_init(bar_base + 8 * (kS + s), hkv);   // empty: one arrive per consumer warp
         }
         fence_barrier_init();
     }
@@ -252,7 +237,7 @@ __global__ void __launch_bounds__((MAX_KV_HEADS * decode_warps_per_kv_head(GQ, M
     fence_proxy_async_smem();   // the zeros must land before any bulk copy writes these bytes
     __syncthreads();
 
-    if (warp == hkv * kWPH) {
+    if (warp == hkv) {
         // ---------------- producer: one lane issues the bulk copies ----------------
         if (lane == 0) {
             const int bs_mask = (1 << p.block_shift) - 1;
@@ -310,13 +295,12 @@ __global__ void __launch_bounds__((MAX_KV_HEADS * decode_warps_per_kv_head(GQ, M
         return;
     }
 
-    // ------- consumers: warp w = kv head w / kWPH, G of its query heads (share w % kWPH) -------
-    const int kvh = warp / kWPH;
-    const int hsub = warp % kWPH;
+    // ---------------- consumers: warp w = kv head w and its G query heads ----------------
+    const int kvh = warp;
     const int half = lane >> 4;
     const int sl = lane & 15;
     constexpr int kLanesPerHead = 16 / G;
-    const int head0 = kvh * GQ + hsub * G;
+    const int head0 = kvh * G;
 
     // Dims are held in pairs and the dot products and accumulations use the packed fp32 pair
     // instructions: each one does the FMAs of two dims.
@@ -413,7 +397,7 @@ __global__ void __launch_bounds__((MAX_KV_HEADS * decode_warps_per_kv_head(GQ, M
             }
         }
         // fused store: this warp writes its kv head of the new row (K by lanes 0-15, V by 16-31)
-        if (kFused && hsub == 0 && new_pos >= t0 + c * kT && new_pos < t0 + c * kT + kT && nvalid > 0) {
+        if (kFused && new_pos >= t0 + c * kT && new_pos < t0 + c * kT + kT && nvalid > 0) {
             const int tok0 = t0 + c * kT;
             const uint32_t src = (half ? vbase : kbase) + (uint32_t)(new_pos - tok0) * row_bytes;
             __nv_bfloat16 *dst = (half ? p.v_cache_w : p.k_cache_w) + new_slot * dkv + kvh * kD + sl * 8;
@@ -488,7 +472,7 @@ __global__ void __launch_bounds__((MAX_KV_HEADS * decode_warps_per_kv_head(GQ, M
         // visible device-wide before its count; on the last split, the fence after the count
         // orders the merge's reads after every other split's partials.)
         __shared__ int s_last;
-        const uint32_t consumers = (uint32_t)(hkv * kWPH) * 32u;
+        const uint32_t consumers = (uint32_t)hkv * 32u;
         asm volatile("bar.sync 1, %0;" ::"r"(consumers) : "memory");
         if (threadIdx.x == 0) {
             __threadfence();
@@ -521,10 +505,49 @@ int decode_split_tokens(int num_seqs, int max_context_len)
     return split;
 }
 
+// The store half of nv_store_decode_attn when its decode runs on the tile kernel: a warp per row
+// writes the new K/V row of sequence b to slot_mapping[b] only when that is the slot of position
+// L-1 through the block table -- the rule the fused CUDA-core kernel applies -- and flags any
+// other slot the same way (the decode then reads position L-1 from the pool).
+__global__ void __launch_bounds__(256) decode_store_kernel(const DecodeParams p, int num_seqs)
+{
+    const int b = blockIdx.x * 8 + (int)(threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (b >= num_seqs)
+        return;
+    const int s = __ldg(p.slot_mapping + b);
+    if (s == -1)
+        return;
+    int L = __ldg(p.context_lens + b);
+    L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);   // as the decode reads it (it flags the length)
+    if (s < -1 || s >= p.num_slots) {
+        if (lane == 0)
+            flag_error(p.d_err, NV_DERR_SLOT_RANGE);
+        return;
+    }
+    const int lp = L - 1;
+    const int blk = L > 0 ? __ldg(p.block_tables + (size_t)b * p.bt_stride + (lp >> p.block_shift)) : -1;
+    const int64_t want = ((int64_t)blk << p.block_shift) + (lp & ((1 << p.block_shift) - 1));
+    if (L == 0 || blk < 0 || blk >= p.num_blocks || want != s) {
+        if (lane == 0)
+            flag_error(p.d_err, NV_DERR_SLOT_MISMATCH);
+        return;
+    }
+    const int row_u4 = p.num_kv_heads * kD / 8;
+    const uint4 *kr = reinterpret_cast<const uint4 *>(p.k_new + (size_t)b * p.k_new_stride);
+    const uint4 *vr = reinterpret_cast<const uint4 *>(p.v_new + (size_t)b * p.v_new_stride);
+    uint4 *kd = reinterpret_cast<uint4 *>(p.k_cache_w + (int64_t)s * p.num_kv_heads * kD);
+    uint4 *vd = reinterpret_cast<uint4 *>(p.v_cache_w + (int64_t)s * p.num_kv_heads * kD);
+    for (int i = lane; i < row_u4; i += 32) {
+        kd[i] = __ldg(kr + i);
+        vd[i] = __ldg(vr + i);
+    }
+}
+
 template <int G, int MAXH, bool kFused>
 int launch_decode(const DecodeParams &p, int num_seqs, cudaStream_t stream)
 {
-    const size_t smem_bytes = decode_smem_bytes(decode_stages(G, MAXH), p.num_kv_heads);
+    const size_t smem_bytes = decode_smem_bytes(kStages, p.num_kv_heads);
     static bool configured = false;   // benign race: every thread sets the same attribute value
     if (!configured) {
         if (cudaFuncSetAttribute(paged_decode_kernel<G, MAXH, kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -533,8 +556,7 @@ int launch_decode(const DecodeParams &p, int num_seqs, cudaStream_t stream)
         configured = true;
     }
     dim3 grid(num_seqs, p.max_splits);
-    constexpr int wph = decode_warps_per_kv_head(G, MAXH);
-    paged_decode_kernel<G, MAXH, kFused><<<grid, (p.num_kv_heads * wph + 1) * 32, smem_bytes, stream>>>(p);
+    paged_decode_kernel<G, MAXH, kFused><<<grid, (p.num_kv_heads + 1) * 32, smem_bytes, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
 
@@ -545,7 +567,6 @@ int dispatch_group(int group, const DecodeParams &p, int num_seqs, cudaStream_t 
     case 1: return launch_decode<1, MAXH, kFused>(p, num_seqs, st);
     case 2: return launch_decode<2, MAXH, kFused>(p, num_seqs, st);
     case 4: return launch_decode<4, MAXH, kFused>(p, num_seqs, st);
-    case 8: return launch_decode<8, MAXH, kFused>(p, num_seqs, st);
     default: return NV_ERR_UNSUPPORTED;
     }
 }
@@ -560,6 +581,17 @@ int dispatch(int group, const DecodeParams &p, int num_seqs, cudaStream_t st)
                  : dispatch_group<16, false>(group, p, num_seqs, st);
 }
 
+// Decode with this many query heads per kv head or more runs on the tcgen05 tile kernel (as a
+// prefill of one query row per sequence): the CUDA-core kernel's warps do G times the FMAs per KV
+// byte and stop keeping up with HBM at G = 8 (measured 0.54 of the HBM roofline there, against
+// about 1.0 for the tile kernel on the same batch).  Its work list sits after the split counters.
+constexpr int kTileGroup = 8;
+
+size_t tile_list_bytes(int32_t num_seqs)
+{
+    return nvkv_host::tile_workspace_bytes(num_seqs, num_seqs, 1, kTileGroup);
+}
+
 }  // namespace
 
 extern "C" size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
@@ -569,12 +601,46 @@ extern "C" size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q
         return 0;
     const int split = decode_split_tokens(num_seqs, max_context_len);
     const int max_splits = (max_context_len + split - 1) / split;
+    const size_t tile = kCounterBytes + tile_list_bytes(num_seqs);
     if (max_splits <= 1)
-        return 0;
-    return kCounterBytes + (size_t)num_seqs * max_splits * num_q_heads * (kD + 2) * sizeof(float);
+        return tile;
+    const size_t part = kCounterBytes + (size_t)num_seqs * max_splits * num_q_heads * (kD + 2) * sizeof(float);
+    return part > tile ? part : tile;
 }
 
 namespace {
+
+// Decode as a tile-kernel prefill of one query row per sequence (sequence b's query is row b, at
+// position L-1): the pre-pass lists one query tile per sequence with keys and zeroes the rows of
+// sequences without.
+int decode_on_tiles(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
+                    int32_t bt_stride, const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
+                    int32_t num_kv_heads, int32_t block_size, int32_t num_blocks, int32_t max_len, float scale,
+                    void *out, void *list, size_t list_bytes, int32_t *d_err, cudaStream_t stream)
+{
+    nvkv_host::TileAttnArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.context_lens = context_lens;
+    a.block_tables = block_tables;
+    a.bt_stride = bt_stride;
+    a.num_seqs = num_seqs;
+    a.total_q = num_seqs;
+    a.max_seqlen_q = 1;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.max_len = max_len;
+    a.scale = scale;
+    a.out = out;
+    a.workspace = list;
+    a.workspace_bytes = list_bytes;
+    a.d_err = d_err;
+    a.stream = stream;
+    return nvkv_host::tile_attention(a);
+}
 
 struct StoreArgs {     // the new rows of a fused store + decode (absent for a plain decode)
     const void *k;
@@ -603,7 +669,7 @@ int decode_entry(const void *q, const void *k_cache, const void *v_cache, const 
     if (num_q_heads % num_kv_heads != 0)
         return NV_ERR_SHAPE;
     const int group = num_q_heads / num_kv_heads;
-    if (num_kv_heads > 16 || (group != 1 && group != 2 && group != 4 && group != 8))
+    if (num_kv_heads > 16 || !(group == 1 || group == 2 || group == 4 || group == 8 || group == 16))
         return NV_ERR_UNSUPPORTED;
     if (!is_pow2(block_size) || block_size < 16 || block_size > 256)
         return NV_ERR_UNSUPPORTED;
@@ -649,6 +715,19 @@ int decode_entry(const void *q, const void *k_cache, const void *v_cache, const 
         p.k_cache_w = static_cast<__nv_bfloat16 *>(const_cast<void *>(k_cache));
         p.v_cache_w = static_cast<__nv_bfloat16 *>(const_cast<void *>(v_cache));
         p.num_slots = (int64_t)num_blocks * block_size;
+    }
+    if (group >= kTileGroup) {
+        if (!workspace || workspace_bytes < kCounterBytes + tile_list_bytes(num_seqs) || !aligned16(workspace))
+            return NV_ERR_WORKSPACE;
+        if (st) {       // the store first, by the fused kernel's rule; then the decode reads the pool
+            decode_store_kernel<<<(num_seqs + 7) / 8, 256, 0, (cudaStream_t)stream>>>(p, num_seqs);
+            if (cudaGetLastError() != cudaSuccess)
+                return NV_ERR_CUDA;
+        }
+        return decode_on_tiles(q, k_cache, v_cache, block_tables, bt_stride, context_lens, num_seqs, num_q_heads,
+                               num_kv_heads, block_size, num_blocks, max_len, scale, out,
+                               static_cast<uint8_t *>(workspace) + kCounterBytes, workspace_bytes - kCounterBytes,
+                               d_err, (cudaStream_t)stream);
     }
     if (p.max_splits > 1) {
         const size_t need = nv_paged_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len);
@@ -753,7 +832,7 @@ extern "C" int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, 
     if (num_q_heads % num_kv_heads != 0)
         return NV_ERR_SHAPE;
     const int group = num_q_heads / num_kv_heads;
-    if (num_kv_heads > 16 || (group != 1 && group != 2 && group != 4 && group != 8))
+    if (num_kv_heads > 16 || !(group == 1 || group == 2 || group == 4 || group == 8 || group == 16))
         return NV_ERR_UNSUPPORTED;
     if (!is_pow2(block_size) || block_size < 16 || block_size > 256)
         return NV_ERR_UNSUPPORTED;
@@ -765,6 +844,15 @@ extern "C" int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, 
         max_context_len = 1;
     const int64_t bt_cap = (int64_t)bt_stride * block_size;
     const int max_len = (int)(bt_cap < max_context_len ? bt_cap : max_context_len);
+    if (group >= kTileGroup) {     // the tile kernel's work list goes in the static array
+        void *scratch = nullptr;
+        int32_t *counters = nullptr;
+        if (!static_arrays(&scratch, &counters))
+            return NV_ERR_CUDA;
+        return decode_on_tiles(q, k_cache, v_cache, block_tables, bt_stride, context_lens, num_seqs, num_q_heads,
+                               num_kv_heads, block_size, num_blocks, max_len, scale, out, scratch,
+                               (size_t)NV_DECODE_STATIC_SCRATCH_BYTES, d_err, (cudaStream_t)stream);
+    }
 
     // The usual split length, doubled until the partials fit in the static array.
     int split = decode_split_tokens(num_seqs, max_context_len);

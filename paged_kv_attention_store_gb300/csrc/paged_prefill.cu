@@ -45,6 +45,7 @@
 #include <type_traits>
 
 #include "nv_common.cuh"
+#include "tile_attention.cuh"
 
 namespace {
 
@@ -243,13 +244,30 @@ constexpr int kPlanHeaderInts = 16;
 struct PlanParams {
     const int32_t *cu_q;
     const int32_t *cu_k;
+    const int32_t *ctx;      // decode mode (cu_q, cu_k unused): context lengths, query row b = sequence b
+    uint4 *out;              // decode mode: rows of sequences with no keys are zeroed here
     int32_t *ws;
     int32_t *d_err;
     int32_t num_seqs, total_q, bt_stride, block_shift, tq, max_tiles, cap;
+    int32_t max_len;         // decode mode: longer contexts are truncated to this (NV_DERR_LENGTH)
+    int32_t row_u4;          // decode mode: 16-byte words per output row
 };
 
 __device__ __forceinline__ bool plan_seq(const PlanParams &pp, int b, int &cq0, int &Lq, int &P, int &T)
 {
+    if (pp.ctx) {
+        // decode: the sequence's one query (row b) sits at position L-1 and sees all L keys
+        int L = pp.ctx[b];
+        if (L < 0 || L > pp.max_len) {
+            flag_error(pp.d_err, NV_DERR_LENGTH);
+            L = L < 0 ? 0 : pp.max_len;
+        }
+        cq0 = b;
+        Lq = L > 0 ? 1 : 0;
+        P = L - Lq;
+        T = Lq;
+        return true;
+    }
     cq0 = pp.cu_q[b];
     const int cq1 = pp.cu_q[b + 1];
     const int Lk = pp.cu_k[b + 1] - pp.cu_k[b];
@@ -338,8 +356,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const Pla
     // (heaviest) tile first
     for (int b = warp; b < pp.num_seqs; b += kPlanThreads / 32) {
         int cq0, Lq, P, T;
-        if (!plan_seq(pp, b, cq0, Lq, P, T) || T == 0)
+        if (!plan_seq(pp, b, cq0, Lq, P, T))
             continue;
+        if (T == 0) {
+            if (pp.ctx)      // decode: a row with no keys (graph padding) attends to nothing: zeros
+                for (int i = lane; i < pp.row_u4; i += 32)
+                    pp.out[(size_t)b * pp.row_u4 + i] = make_uint4(0, 0, 0, 0);
+            continue;
+        }
         int first = 0;
         if (lane == 0)
             first = atomicAdd(&hist[seq_bucket(P, Lq, T, pp.tq)], T);
@@ -973,6 +997,11 @@ size_t prefill_workspace_bytes(int64_t cap)
 }
 }  // namespace
 
+size_t nvkv_host::tile_workspace_bytes(int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q, int group)
+{
+    return prefill_workspace_bytes(prefill_entries_cap(num_seqs, total_q, max_seqlen_q, group));
+}
+
 extern "C" size_t nv_paged_prefill_workspace_size(int32_t num_seqs, int32_t total_q, int32_t max_seqlen_q,
                                                   int32_t num_q_heads, int32_t num_kv_heads)
 {
@@ -983,6 +1012,111 @@ extern "C" size_t nv_paged_prefill_workspace_size(int32_t num_seqs, int32_t tota
     if (group > kBM)
         return (size_t)kPlanHeaderInts * 4u;
     return prefill_workspace_bytes(prefill_entries_cap(num_seqs, total_q, max_seqlen_q, group));
+}
+
+int nvkv_host::tile_attention(const TileAttnArgs &a)
+{
+    using namespace nvkv_host;
+    const int num_q_heads = a.num_q_heads, num_kv_heads = a.num_kv_heads, block_size = a.block_size;
+    const int num_seqs = a.num_seqs, total_q = a.total_q, max_seqlen_q = a.max_seqlen_q, num_blocks = a.num_blocks;
+    const int group = num_q_heads / num_kv_heads;
+    if (!is_pow2(group) || group > 16 || num_kv_heads > 65535)
+        return NV_ERR_UNSUPPORTED;
+    if (!is_pow2(block_size) || block_size < 16 || block_size > 256)
+        return NV_ERR_UNSUPPORTED;
+    if ((int64_t)num_blocks * block_size >= (1ll << 31) || num_seqs > 65535)
+        return NV_ERR_UNSUPPORTED;
+    if (!aligned16(a.q) || !aligned16(a.k_cache) || !aligned16(a.v_cache) || !aligned16(a.out))
+        return NV_ERR_ALIGN;
+    if (num_blocks == 0)
+        return NV_ERR_SHAPE;
+    const int64_t cap = prefill_entries_cap(num_seqs, total_q, max_seqlen_q, group);
+    if (cap * num_kv_heads >= (1ll << 31))
+        return NV_ERR_UNSUPPORTED;
+    if (!a.workspace || a.workspace_bytes < prefill_workspace_bytes(cap) || !aligned16(a.workspace))
+        return NV_ERR_WORKSPACE;
+
+    const int box_rows = block_size < kBN ? block_size : kBN;
+    const int tq = kBM / group;
+    CUtensorMap tq_map, tk, tv, to;
+    const int64_t num_slots = (int64_t)num_blocks * block_size;
+    if (!make_map(&tq_map, a.q, total_q, num_q_heads, group, tq) ||
+        !make_map(&tk, a.k_cache, num_slots, num_kv_heads, 1, box_rows) ||
+        !make_map(&tv, a.v_cache, num_slots, num_kv_heads, 1, box_rows) ||
+        !make_map(&to, a.out, total_q, num_q_heads, group, 32 / group))
+        return NV_ERR_CUDA;
+
+    PrefillParams p{};
+    p.out = static_cast<__nv_bfloat16 *>(a.out);
+    p.block_tables = a.block_tables;
+    p.d_err = a.d_err;
+    p.bt_stride = a.bt_stride;
+    p.num_q_heads = num_q_heads;
+    p.group = group;
+    p.group_shift = ilog2(group);
+    p.block_shift = ilog2(block_size);
+    p.box_rows = box_rows;
+    p.num_blocks = num_blocks;
+    p.num_kv_heads = num_kv_heads;
+    p.scale_log2 = a.scale * nvkv::kLog2e;
+    p.ws = static_cast<int32_t *>(a.workspace);
+
+    PlanParams pp{};
+    pp.cu_q = a.cu_seqlens_q;
+    pp.cu_k = a.cu_seqlens_k;
+    pp.ctx = a.context_lens;
+    pp.out = static_cast<uint4 *>(a.out);
+    pp.ws = p.ws;
+    pp.d_err = a.d_err;
+    pp.num_seqs = num_seqs;
+    pp.total_q = total_q;
+    pp.bt_stride = a.bt_stride;
+    pp.block_shift = p.block_shift;
+    pp.tq = tq;
+    pp.max_tiles = (max_seqlen_q + tq - 1) / tq;
+    pp.cap = (int32_t)cap;
+    pp.max_len = a.max_len;
+    pp.row_u4 = num_q_heads * kD / 8;
+    const int sms = sm_count();
+    if (sms <= 0)
+        return NV_ERR_CUDA;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    static bool regs_ok = false;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(paged_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        // the warpgroups' register split (setmaxnreg) adds up to exactly the launch budget: refuse to
+        // launch a build whose per-thread register count differs, rather than let a warpgroup wait
+        // for registers that never come
+        cudaFuncAttributes fa{};
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncGetAttributes(&fa, paged_prefill_kernel);
+        regs_ok = attr_err == cudaSuccess && fa.numRegs == kLaunchRegs;
+    });
+    if (attr_err != cudaSuccess)
+        return NV_ERR_CUDA;
+    if (!regs_ok)
+        return NV_ERR_UNSUPPORTED;
+    prefill_plan_kernel<<<1, kPlanThreads, 0, a.stream>>>(pp);
+    // persistent: one CTA per SM (shared memory and TMEM admit one); CTAs claim the work list's
+    // entries in order
+    const int64_t claims = cap * num_kv_heads;
+    const int grid = (int)(claims < sms ? claims : sms);
+    // launched as a programmatic dependent of the pre-pass: its CTAs set up (barriers, TMEM, tensor
+    // maps) while the pre-pass runs, and wait for the work list with griddepcontrol.wait
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, paged_prefill_kernel, tq_map, tk, tv, to, p) != cudaSuccess)
+        return NV_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
 
 extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const void *v_cache,
@@ -1005,99 +1139,26 @@ extern "C" int nv_paged_prefill_attn(const void *q, const void *k_cache, const v
         return NV_ERR_UNSUPPORTED;
     if (num_q_heads % num_kv_heads != 0)
         return NV_ERR_SHAPE;
-    const int group = num_q_heads / num_kv_heads;
-    if (!is_pow2(group) || group > 16 || num_kv_heads > 65535)
-        return NV_ERR_UNSUPPORTED;
-    if (!is_pow2(block_size) || block_size < 16 || block_size > 256)
-        return NV_ERR_UNSUPPORTED;
-    if ((int64_t)num_blocks * block_size >= (1ll << 31) || num_seqs > 65535)
-        return NV_ERR_UNSUPPORTED;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-        return NV_ERR_ALIGN;
-    if (num_blocks == 0)
-        return NV_ERR_SHAPE;
-    const int64_t cap = prefill_entries_cap(num_seqs, total_q, max_seqlen_q, group);
-    if (cap * num_kv_heads >= (1ll << 31))
-        return NV_ERR_UNSUPPORTED;
-    if (!workspace || workspace_bytes < prefill_workspace_bytes(cap) || !aligned16(workspace))
-        return NV_ERR_WORKSPACE;
-
-    const int box_rows = block_size < kBN ? block_size : kBN;
-    const int tq = kBM / group;
-    CUtensorMap tq_map, tk, tv, to;
-    const int64_t num_slots = (int64_t)num_blocks * block_size;
-    if (!make_map(&tq_map, q, total_q, num_q_heads, group, tq) ||
-        !make_map(&tk, k_cache, num_slots, num_kv_heads, 1, box_rows) ||
-        !make_map(&tv, v_cache, num_slots, num_kv_heads, 1, box_rows) ||
-        !make_map(&to, out, total_q, num_q_heads, group, 32 / group))
-        return NV_ERR_CUDA;
-
-    PrefillParams p{};
-    p.out = static_cast<__nv_bfloat16 *>(out);
-    p.block_tables = block_tables;
-    p.d_err = d_err;
-    p.bt_stride = bt_stride;
-    p.num_q_heads = num_q_heads;
-    p.group = group;
-    p.group_shift = ilog2(group);
-    p.block_shift = ilog2(block_size);
-    p.box_rows = box_rows;
-    p.num_blocks = num_blocks;
-    p.num_kv_heads = num_kv_heads;
-    p.scale_log2 = scale * nvkv::kLog2e;
-    p.ws = static_cast<int32_t *>(workspace);
-
-    PlanParams pp{};
-    pp.cu_q = cu_seqlens_q;
-    pp.cu_k = cu_seqlens_k;
-    pp.ws = p.ws;
-    pp.d_err = d_err;
-    pp.num_seqs = num_seqs;
-    pp.total_q = total_q;
-    pp.bt_stride = bt_stride;
-    pp.block_shift = p.block_shift;
-    pp.tq = tq;
-    pp.max_tiles = (max_seqlen_q + tq - 1) / tq;
-    pp.cap = (int32_t)cap;
-
-    const int sms = sm_count();
-    if (sms <= 0)
-        return NV_ERR_CUDA;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    static bool regs_ok = false;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(paged_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        // the warpgroups' register split (setmaxnreg) adds up to exactly the launch budget: refuse to
-        // launch a build whose per-thread register count differs, rather than let a warpgroup wait
-        // for registers that never come
-        cudaFuncAttributes fa{};
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncGetAttributes(&fa, paged_prefill_kernel);
-        regs_ok = attr_err == cudaSuccess && fa.numRegs == kLaunchRegs;
-    });
-    if (attr_err != cudaSuccess)
-        return NV_ERR_CUDA;
-    if (!regs_ok)
-        return NV_ERR_UNSUPPORTED;
-    prefill_plan_kernel<<<1, kPlanThreads, 0, (cudaStream_t)stream>>>(pp);
-    // persistent: one CTA per SM (shared memory and TMEM admit one); CTAs claim the work list's
-    // entries in order
-    const int64_t claims = cap * num_kv_heads;
-    const int grid = (int)(claims < sms ? claims : sms);
-    // launched as a programmatic dependent of the pre-pass: its CTAs set up (barriers, TMEM, tensor
-    // maps) while the pre-pass runs, and wait for the work list with griddepcontrol.wait
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = (cudaStream_t)stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, paged_prefill_kernel, tq_map, tk, tv, to, p) != cudaSuccess)
-        return NV_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
+    TileAttnArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.cu_seqlens_q = cu_seqlens_q;
+    a.cu_seqlens_k = cu_seqlens_k;
+    a.block_tables = block_tables;
+    a.bt_stride = bt_stride;
+    a.num_seqs = num_seqs;
+    a.total_q = total_q;
+    a.max_seqlen_q = max_seqlen_q;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.block_size = block_size;
+    a.num_blocks = num_blocks;
+    a.scale = scale;
+    a.out = out;
+    a.workspace = workspace;
+    a.workspace_bytes = workspace_bytes;
+    a.d_err = d_err;
+    a.stream = (cudaStream_t)stream;
+    return tile_attention(a);
 }

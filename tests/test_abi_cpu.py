@@ -84,7 +84,12 @@ def test_decode_validation(lib):
     assert need > 0
     assert _decode(lib) == NV_ERR_WORKSPACE
     assert _decode(lib, ws=FAKE, wsb=need - 16) == NV_ERR_WORKSPACE
-    assert lib.nv_paged_decode_workspace_size(4, 32, 128, 64) == 0   # one split: no workspace
+    # one split: no partials, but room for the tile kernel's work list (groups of 8 and 16) after the
+    # 256 KiB of counters (64 bytes + 32 per sequence)
+    assert lib.nv_paged_decode_workspace_size(4, 32, 128, 64) == 256 * 1024 + 64 + 32 * 4
+    assert _decode(lib, hq=128, hkv=8) == NV_ERR_WORKSPACE     # group 16: the tile kernel, needs the list
+    assert _decode(lib, hq=128, hkv=8, maxc=64, ws=FAKE, wsb=256 * 1024 + 64) == NV_ERR_WORKSPACE
+    assert _decode(lib, hq=256, hkv=8) == NV_ERR_UNSUPPORTED   # group 32
 
 
 def test_decode_workspace_size_follows_the_split_rule(lib):
@@ -108,6 +113,8 @@ def _fused(lib, q=FAKE, k=FAKE, ks=1024, v=FAKE, vs=1024, sm=FAKE, kc=FAKE, vc=F
 
 def test_fused_store_decode_validation(lib):
     assert _fused(lib, B=0, q=None) == 0
+    assert _fused(lib, hq=128, hkv=8) == NV_ERR_WORKSPACE      # group 16: store + tile kernel, needs the list
+    assert _fused(lib, hq=256, hkv=8) == NV_ERR_UNSUPPORTED    # group 32
     assert _fused(lib, k=None) == NV_ERR_NULL
     assert _fused(lib, sm=None) == NV_ERR_NULL
     assert _fused(lib, q=None) == NV_ERR_NULL

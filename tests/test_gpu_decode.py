@@ -194,3 +194,44 @@ def test_decode_workspace_not_zero_filled_is_flagged():
     nv.nv_paged_decode_attn(db.q, db.k_cache, db.v_cache, db.block_tables, db.seq_lens, b.scale,
                             max_context_len=4096, workspace=ws, d_err=db.d_err)
     assert db.err() & nv.NV_DERR_VALUE
+
+
+# ---- groups of 8 and 16 query heads per kv head: the tcgen05 tile kernel (one query row per sequence) ----
+
+@pytest.mark.parametrize("hq,hkv,bs", [(128, 8, 256), (16, 1, 16), (64, 4, 64)], ids=["g16-hkv8", "g16-hkv1", "g16-hkv4"])
+def test_decode_group16(hq, hkv, bs):
+    b = W.make_decode(f"g16-{hq}-{hkv}", 30, [1, 2, 127, 128, 129, 2000, 4100], hq, hkv, 128, bs, n_pad=2,
+                      poison_tail=True)
+    db, got, kc, vc = _run(b)
+    compare(got, oracle_decode(oracle.default(), b, kc, vc), b.name)
+    assert not got[b.seq_lens == 0].any()
+
+
+def test_decode_group8_length_beyond_hint_is_truncated_and_flagged():
+    """As on the split-KV kernel: a context longer than the host hint attends to its first
+    max_context_len keys and NV_DERR_LENGTH is set; the other rows are unaffected."""
+    import paged_kv_attention_store_gb300 as nv
+    b = W.make_decode("len8", 31, [40, 300, 90], 64, 8, 128, 16, n_pad=1)
+    db = DeviceBatch(b)
+    db.store()
+    got = host_f32(db.decode(max_context_len=100))
+    assert db.err() & nv.NV_DERR_LENGTH
+    kc, vc = oracle_cache_after_store(oracle.default(), b, db.kc_host0, db.vc_host0)
+    cut = W.PagedBatch(**{**b.__dict__, "seq_lens": np.minimum(b.seq_lens, 100).astype(np.int32)})
+    compare(got, oracle_decode(oracle.default(), cut, kc, vc), "truncated")
+    assert not got[3].any()
+
+
+def test_decode_group8_bad_block_id_is_flagged_not_faulted():
+    import paged_kv_attention_store_gb300 as nv
+    b = W.make_decode("badblk8", 32, [400, 20], 64, 8, 128, 16)
+    bt = b.block_tables.copy()
+    bt[0, 3] = b.num_blocks + 7
+    b2 = W.PagedBatch(**{**b.__dict__, "block_tables": bt})
+    db = DeviceBatch(b2)
+    got = host_f32(db.decode())
+    assert db.err() & nv.NV_DERR_BLOCK_RANGE
+    # the sequence without a bad entry is unaffected (the oracle runs on the valid tables: row 1's is
+    # the same in both)
+    want = oracle_decode(oracle.default(), b, db.kc_host0, db.vc_host0)
+    compare(got[1:2], want[1:2], "unaffected row")

@@ -38,7 +38,17 @@ def _call(f, db, out, max_ctx):
              max_ctx, b.scale, out.data_ptr(), db.d_err.data_ptr(), torch.cuda.current_stream().cuda_stream)
 
 
-@pytest.mark.parametrize("make", [W.qwen06_decode, W.qwen8_decode], ids=["qwen3-0.6b", "qwen3-8b"])
+def _group8():
+    ctx = np.random.default_rng([0, 200]).integers(1024, 4097, size=96)
+    return W.make_decode("group8", 3, ctx, 64, 8, 128, 256, n_pad=5)
+
+
+def _group16():
+    return W.make_decode("group16", 4, [1, 300, 2048, 700], 128, 8, 128, 16, n_pad=2)
+
+
+@pytest.mark.parametrize("make", [W.qwen06_decode, W.qwen8_decode, _group8, _group16],
+                         ids=["qwen3-0.6b", "qwen3-8b", "group8-tiles", "group16-tiles"])
 def test_noalloc_matches_allocating_entry_point_twice(make):
     import torch
     b = make()
@@ -59,9 +69,10 @@ def test_noalloc_matches_allocating_entry_point_twice(make):
 
 
 def test_noalloc_rejects_a_batch_beyond_the_static_array():
-    """1024 sequences x 64 heads x 8192 positions need more partials than the array holds even at the
-    longest split: rejected on the host, nothing enqueued (the pointers are never touched)."""
+    """1024 sequences x 64 q heads (16 kv heads: group 4, the split-KV kernel) x 8192 positions need
+    more partials than the array holds even at the longest split: rejected on the host, nothing
+    enqueued (the pointers are never touched)."""
     f = _c_entry()
     fake = 0x10000
-    rc = f(fake, fake, fake, fake, 32, fake, 1024, 64, 8, 128, 256, 64, 8192, 0.088, fake, None, None)
+    rc = f(fake, fake, fake, fake, 32, fake, 1024, 64, 16, 128, 256, 64, 8192, 0.088, fake, None, None)
     assert rc == NV_ERR_WORKSPACE
