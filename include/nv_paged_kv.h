@@ -207,7 +207,7 @@ size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
  * A row with L == 0 (graph padding) gets zeros.
  *
  * Groups (num_q_heads / num_kv_heads) 1, 2, 4: a split-KV flash-decoding kernel on CUDA cores (one
- * launch).  Groups 8 and 16: each query head of a group multiplies every KV byte, and the CUDA-core
+ * launch; a second one merges the partials when a sequence spans more than 16 splits).  Groups 8 and 16: each query head of a group multiplies every KV byte, and the CUDA-core
  * kernel's FMAs no longer keep up with HBM (measured 0.54 of the roofline at group 8), so the call
  * runs the tcgen05 tile kernel of nv_paged_prefill_attn with one query row per sequence at position
  * L-1 (two launches: a work-list pre-pass, which also zeroes the rows with L == 0, and the tile

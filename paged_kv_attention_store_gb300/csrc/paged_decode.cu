@@ -67,6 +67,7 @@ struct DecodeParams {
     int32_t max_len;    // min(max_context_len, bt_stride * block_size)
     int32_t split_tokens;
     int32_t max_splits;
+    int32_t merge_in_kernel;   // 1: a sequence's last split merges; 0: merge_splits_kernel follows
     float scale_log2;   // scale * log2(e)
     // fused store (nv_store_decode_attn); k_new == nullptr for a plain decode
     const __nv_bfloat16 *k_new;     // [num_seqs, Hkv, 128], rows k_new_stride elements apart
@@ -147,6 +148,73 @@ __device__ __forceinline__ void merge_splits(const DecodeParams &p, int b, int n
         w2.x = pack_bf16x2(n0 * inv, n1 * inv);
         w2.y = pack_bf16x2(n2 * inv, n3 * inv);
         *reinterpret_cast<uint2 *>(p.out + ((size_t)b * p.num_q_heads + h) * kD + d4 * 4) = w2;
+    }
+}
+
+// Sequences with more splits than this merge in merge_splits_kernel after the split launch: the
+// in-kernel merge runs on one CTA, whose loop over the splits is bound by L2 latency (one 32K-token
+// sequence in 512 splits of 64 positions took 275 us, nearly all of it that merge).
+constexpr int kFusedMergeMaxSplits = 16;
+
+// The split partials of sequence blockIdx.x, query head blockIdx.y, combined as in merge_splits: warp
+// w takes splits w, w+4, ..., lane l dims 4l..4l+3, and the four warps' sums meet in shared memory.
+__global__ void __launch_bounds__(128) merge_splits_kernel(const DecodeParams p)
+{
+    const int b = blockIdx.x, h = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int L = __ldg(p.context_lens + b);
+    L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);      // as the split launch read it (it flags)
+    const int nsplit = (L + p.split_tokens - 1) / p.split_tokens;
+    if (nsplit <= 1)
+        return;                   // written directly by its one split (zeros for L == 0)
+    const float *ml = p.part_ml + ((size_t)b * p.max_splits * p.num_q_heads + h) * 2;
+    const float *po = p.part_o + ((size_t)b * p.max_splits * p.num_q_heads + h) * kD + lane * 4;
+    const size_t split_ml = (size_t)p.num_q_heads * 2, split_o = (size_t)p.num_q_heads * kD;
+    __shared__ float s_m[4];
+    __shared__ float4 s_n[4][32];
+    __shared__ float s_den[4];
+    float M = -INFINITY;
+    for (int sp = threadIdx.x; sp < nsplit; sp += 128)
+        M = fmaxf(M, ml[sp * split_ml]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (lane == 0)
+        s_m[warp] = M;
+    __syncthreads();
+    M = fmaxf(fmaxf(s_m[0], s_m[1]), fmaxf(s_m[2], s_m[3]));
+    float den = 0.f;
+    float4 n = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int sp = warp; sp < nsplit; sp += 4) {
+        const float2 m_l = *reinterpret_cast<const float2 *>(ml + sp * split_ml);
+        const float4 o = *reinterpret_cast<const float4 *>(po + sp * split_o);
+        const float w = (m_l.x == -INFINITY) ? 0.f : fast_exp2(m_l.x - M);
+        den = fmaf(w, m_l.y, den);
+        n.x = fmaf(w, o.x, n.x);
+        n.y = fmaf(w, o.y, n.y);
+        n.z = fmaf(w, o.z, n.z);
+        n.w = fmaf(w, o.w, n.w);
+    }
+    s_n[warp][lane] = n;
+    if (lane == 0)
+        s_den[warp] = den;
+    __syncthreads();
+    if (warp == 0) {
+        float4 t = s_n[0][lane];
+        for (int w2 = 1; w2 < 4; ++w2) {
+            const float4 u = s_n[w2][lane];
+            t.x += u.x;
+            t.y += u.y;
+            t.z += u.z;
+            t.w += u.w;
+        }
+        const float d = s_den[0] + s_den[1] + s_den[2] + s_den[3];
+        const float inv = d > 0.f ? 1.f / d : 0.f;
+        uint2 w2;
+        w2.x = pack_bf16x2(t.x * inv, t.y * inv);
+        w2.y = pack_bf16x2(t.z * inv, t.w * inv);
+        *reinterpret_cast<uint2 *>(p.out + ((size_t)b * p.num_q_heads + h) * kD + lane * 4) = w2;
     }
 }
 
@@ -465,6 +533,8 @@ __global__ void __launch_bounds__((MAX_KV_HEADS + 1) * 32, MAX_KV_HEADS <= 8 ? 2
                         make_float2(m_g[g], l_g[g]);
             }
         }
+        if (!p.merge_in_kernel)
+            return;           // many splits: merge_splits_kernel combines them after this launch
         // Count this split as done (its partials made visible first); the sequence's last split
         // to get here merges them all.  Every CTA with t0 < L reaches this point exactly once,
         // whatever happened in its loop, so the counter always reaches nsplit and is reset.
@@ -579,6 +649,18 @@ int dispatch(int group, const DecodeParams &p, int num_seqs, cudaStream_t st)
                      : dispatch_group<8, false>(group, p, num_seqs, st);
     return fused ? dispatch_group<16, true>(group, p, num_seqs, st)
                  : dispatch_group<16, false>(group, p, num_seqs, st);
+}
+
+// The split launch; with more than kFusedMergeMaxSplits splits, then a merge launch over
+// (sequence, query head).
+int run_split_kv(int group, DecodeParams &p, int num_seqs, cudaStream_t st)
+{
+    p.merge_in_kernel = p.max_splits <= kFusedMergeMaxSplits ? 1 : 0;
+    const int rc = dispatch(group, p, num_seqs, st);
+    if (rc != NV_OK || p.merge_in_kernel)
+        return rc;
+    merge_splits_kernel<<<dim3(num_seqs, p.num_q_heads), 128, 0, st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
 
 // Decode with this many query heads per kv head or more runs on the tcgen05 tile kernel (as a
@@ -739,7 +821,7 @@ int decode_entry(const void *q, const void *k_cache, const void *v_cache, const 
         p.part_o = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kCounterBytes);
         p.part_ml = p.part_o + (size_t)num_seqs * p.max_splits * num_q_heads * kD;
     }
-    return dispatch(group, p, num_seqs, (cudaStream_t)stream);
+    return run_split_kv(group, p, num_seqs, (cudaStream_t)stream);
 }
 
 }  // namespace
@@ -893,5 +975,5 @@ extern "C" int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, 
         p.part_o = static_cast<float *>(scratch);
         p.part_ml = p.part_o + (size_t)num_seqs * p.max_splits * num_q_heads * kD;
     }
-    return dispatch(group, p, num_seqs, (cudaStream_t)stream);
+    return run_split_kv(group, p, num_seqs, (cudaStream_t)stream);
 }

@@ -183,16 +183,18 @@ def test_decode_workspace_reused_across_batches_and_after_an_error():
 
 
 def test_decode_workspace_not_zero_filled_is_flagged():
-    """Split counters that do not start at zero (a workspace that was not zero-filled) are reported."""
+    """Split counters that do not start at zero (a workspace that was not zero-filled) are reported.
+    100 sequences of 1024 positions split 8 ways, so the last split of each merges in the kernel
+    through the counters (above 16 splits a merge launch combines them, and no counter is used)."""
     import torch
     import paged_kv_attention_store_gb300 as nv
-    b = W.make_decode("dirty-ws", 29, [4096, 3000, 2500], 32, 8, 128, 64)
+    b = W.make_decode("dirty-ws", 29, [1024] * 100, 8, 2, 128, 64)
     db = DeviceBatch(b)
     db.store()
-    ws = torch.full((nv.nv_paged_decode_workspace_size(b.num_seqs, 32, 128, 4096),), 0xFF, dtype=torch.uint8,
+    ws = torch.full((nv.nv_paged_decode_workspace_size(b.num_seqs, 8, 128, 1024),), 0xFF, dtype=torch.uint8,
                     device="cuda")
     nv.nv_paged_decode_attn(db.q, db.k_cache, db.v_cache, db.block_tables, db.seq_lens, b.scale,
-                            max_context_len=4096, workspace=ws, d_err=db.d_err)
+                            max_context_len=1024, workspace=ws, d_err=db.d_err)
     assert db.err() & nv.NV_DERR_VALUE
 
 
