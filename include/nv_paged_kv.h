@@ -211,7 +211,9 @@ size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
  * kernel's FMAs no longer keep up with HBM (measured 0.54 of the roofline at group 8), so the call
  * runs the tcgen05 tile kernel of nv_paged_prefill_attn with one query row per sequence at position
  * L-1 (two launches: a work-list pre-pass, which also zeroes the rows with L == 0, and the tile
- * kernel).  The two paths round differently (both within the parity bar of the fp32 definition).
+ * kernel; a batch with fewer than two (sequence, kv head) units per SM has its keys split into
+ * ranges of at least 1024, and a third launch merges them).  The two paths round differently (both
+ * within the parity bar of the fp32 definition).
  *
  *   q, out        bf16 [num_seqs, num_q_heads, head_dim], contiguous, 16-byte aligned.
  *   block_tables  int32 [num_seqs, bt_stride]; context_lens int32 [num_seqs].

@@ -676,6 +676,10 @@ size_t tile_list_bytes(int32_t num_seqs)
 
 }  // namespace
 
+// 256 KiB of split counters, then the partials of the split-KV kernel's splits, then room for the
+// tile kernel's work list at that many entries per sequence.  The tile kernel splits a sequence
+// only into ranges of at least 1024 keys, never shorter than the split-KV kernel's, so its
+// partials and list fit the same space.
 extern "C" size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
                                                  int32_t max_context_len)
 {
@@ -683,11 +687,8 @@ extern "C" size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q
         return 0;
     const int split = decode_split_tokens(num_seqs, max_context_len);
     const int max_splits = (max_context_len + split - 1) / split;
-    const size_t tile = kCounterBytes + tile_list_bytes(num_seqs);
-    if (max_splits <= 1)
-        return tile;
-    const size_t part = kCounterBytes + (size_t)num_seqs * max_splits * num_q_heads * (kD + 2) * sizeof(float);
-    return part > tile ? part : tile;
+    const size_t part = max_splits <= 1 ? 0 : (size_t)num_seqs * max_splits * num_q_heads * (kD + 2) * sizeof(float);
+    return kCounterBytes + part + tile_list_bytes((int32_t)((int64_t)num_seqs * (max_splits > 1 ? max_splits : 1)));
 }
 
 namespace {
@@ -695,11 +696,51 @@ namespace {
 // Decode as a tile-kernel prefill of one query row per sequence (sequence b's query is row b, at
 // position L-1): the pre-pass lists one query tile per sequence with keys and zeroes the rows of
 // sequences without.
+//
+// The tile kernel takes a (sequence, kv head) unit's keys in one CTA, so a batch with fewer than two
+// units per SM (a few long contexts) is split into key ranges: enough splits for about three units
+// per SM, each at least 8 key steps (1024 keys) long.  Splits write fp32 partials, and
+// merge_splits_kernel combines them as it does the split-KV kernel's.
+constexpr int kTileMinSplitSteps = 8;
+
+int tile_split_steps(int num_seqs, int num_kv_heads, int max_len)
+{
+    const int64_t units = (int64_t)num_seqs * num_kv_heads;
+    const int sms = nvkv_host::sm_count();
+    const int steps = (max_len + 127) / 128;
+    if (sms <= 0 || units >= 2 * (int64_t)sms || steps <= kTileMinSplitSteps)
+        return 0;
+    const int64_t want = (3 * (int64_t)sms + units - 1) / units;     // splits per sequence
+    int s = (int)((steps + want - 1) / want);
+    if (s < kTileMinSplitSteps)
+        s = kTileMinSplitSteps;
+    return s >= steps ? 0 : s;
+}
+
 int decode_on_tiles(const void *q, const void *k_cache, const void *v_cache, const int32_t *block_tables,
                     int32_t bt_stride, const int32_t *context_lens, int32_t num_seqs, int32_t num_q_heads,
                     int32_t num_kv_heads, int32_t block_size, int32_t num_blocks, int32_t max_len, float scale,
-                    void *out, void *list, size_t list_bytes, int32_t *d_err, cudaStream_t stream)
+                    void *scratch, size_t scratch_bytes, int32_t *d_err, cudaStream_t stream, void *out)
 {
+    // scratch: [partials O][partials (max, sum)][work list]; the split grows until they fit
+    int split_steps = tile_split_steps(num_seqs, num_kv_heads, max_len);
+    int max_splits = 0;
+    size_t part_bytes = 0;
+    while (split_steps > 0) {
+        max_splits = (((max_len + 127) / 128) + split_steps - 1) / split_steps;
+        part_bytes = ((size_t)num_seqs * max_splits * num_q_heads * (kD + 2) * sizeof(float) + 15) & ~(size_t)15;
+        if (part_bytes + tile_list_bytes((int32_t)((int64_t)num_seqs * max_splits)) <= scratch_bytes)
+            break;
+        split_steps *= 2;
+        if (split_steps * 128 >= max_len)
+            split_steps = 0;
+    }
+    if (split_steps == 0) {
+        max_splits = 0;
+        part_bytes = 0;
+    }
+    float *part_o = static_cast<float *>(scratch);
+    float *part_ml = part_o + (size_t)num_seqs * max_splits * num_q_heads * kD;
     nvkv_host::TileAttnArgs a{};
     a.q = q;
     a.k_cache = k_cache;
@@ -715,13 +756,30 @@ int decode_on_tiles(const void *q, const void *k_cache, const void *v_cache, con
     a.block_size = block_size;
     a.num_blocks = num_blocks;
     a.max_len = max_len;
+    a.split_steps = split_steps;
+    a.max_splits = max_splits;
+    a.part_o = split_steps ? part_o : nullptr;
+    a.part_ml = split_steps ? part_ml : nullptr;
     a.scale = scale;
     a.out = out;
-    a.workspace = list;
-    a.workspace_bytes = list_bytes;
+    a.workspace = static_cast<uint8_t *>(scratch) + part_bytes;
+    a.workspace_bytes = scratch_bytes - part_bytes;
     a.d_err = d_err;
     a.stream = stream;
-    return nvkv_host::tile_attention(a);
+    const int rc = nvkv_host::tile_attention(a);
+    if (rc != NV_OK || split_steps == 0)
+        return rc;
+    DecodeParams mp{};
+    mp.context_lens = context_lens;
+    mp.out = static_cast<__nv_bfloat16 *>(out);
+    mp.part_o = part_o;
+    mp.part_ml = part_ml;
+    mp.num_q_heads = num_q_heads;
+    mp.max_len = max_len;
+    mp.split_tokens = split_steps * 128;
+    mp.max_splits = max_splits;
+    merge_splits_kernel<<<dim3(num_seqs, num_q_heads), 128, 0, stream>>>(mp);
+    return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
 
 struct StoreArgs {     // the new rows of a fused store + decode (absent for a plain decode)
@@ -807,9 +865,9 @@ int decode_entry(const void *q, const void *k_cache, const void *v_cache, const 
                 return NV_ERR_CUDA;
         }
         return decode_on_tiles(q, k_cache, v_cache, block_tables, bt_stride, context_lens, num_seqs, num_q_heads,
-                               num_kv_heads, block_size, num_blocks, max_len, scale, out,
+                               num_kv_heads, block_size, num_blocks, max_len, scale,
                                static_cast<uint8_t *>(workspace) + kCounterBytes, workspace_bytes - kCounterBytes,
-                               d_err, (cudaStream_t)stream);
+                               d_err, (cudaStream_t)stream, out);
     }
     if (p.max_splits > 1) {
         const size_t need = nv_paged_decode_workspace_size(num_seqs, num_q_heads, head_dim, max_context_len);
@@ -932,8 +990,8 @@ extern "C" int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, 
         if (!static_arrays(&scratch, &counters))
             return NV_ERR_CUDA;
         return decode_on_tiles(q, k_cache, v_cache, block_tables, bt_stride, context_lens, num_seqs, num_q_heads,
-                               num_kv_heads, block_size, num_blocks, max_len, scale, out, scratch,
-                               (size_t)NV_DECODE_STATIC_SCRATCH_BYTES, d_err, (cudaStream_t)stream);
+                               num_kv_heads, block_size, num_blocks, max_len, scale, scratch,
+                               (size_t)NV_DECODE_STATIC_SCRATCH_BYTES, d_err, (cudaStream_t)stream, out);
     }
 
     // The usual split length, doubled until the partials fit in the static array.

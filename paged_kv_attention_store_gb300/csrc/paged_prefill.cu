@@ -120,6 +120,13 @@ struct PrefillParams {
     int32_t num_kv_heads;
     int32_t *ws;            // work list written by the pre-pass: [0] claim counter, [1] entries
     float scale_log2;
+    // decode split over key ranges (split_steps > 0): an item of a sequence with more than
+    // split_steps key steps writes unnormalised fp32 partials (O, and the row's max and sum in the
+    // log2 domain) for a merge launch instead of bf16 rows
+    int32_t split_steps;
+    int32_t max_splits;
+    float *part_o;          // [num_seqs, max_splits, num_q_heads, 128]
+    float *part_ml;         // [num_seqs, max_splits, num_q_heads, 2]
 };
 
 // ---- packed fp32x2 arithmetic (Blackwell: one instruction for two fp32 lanes) ----
@@ -222,6 +229,7 @@ __device__ __forceinline__ float exp_pack64(const float (&s)[64], float scale_lo
 struct Item {
     int v;                  // claim number; >= total marks the end of the work
     int b, kvh, cq0, Lq, P, i0, nq, kv_len, nkv, first_masked;
+    int n0;                 // first key step (a decode split's key range starts there)
 };
 
 // ---------------------------------------------------------------------------------------
@@ -251,6 +259,7 @@ struct PlanParams {
     int32_t num_seqs, total_q, bt_stride, block_shift, tq, max_tiles, cap;
     int32_t max_len;         // decode mode: longer contexts are truncated to this (NV_DERR_LENGTH)
     int32_t row_u4;          // decode mode: 16-byte words per output row
+    int32_t split_steps;     // decode mode: key steps per entry (0: one entry per sequence)
 };
 
 __device__ __forceinline__ bool plan_seq(const PlanParams &pp, int b, int &cq0, int &Lq, int &P, int &T)
@@ -265,7 +274,8 @@ __device__ __forceinline__ bool plan_seq(const PlanParams &pp, int b, int &cq0, 
         cq0 = b;
         Lq = L > 0 ? 1 : 0;
         P = L - Lq;
-        T = Lq;
+        const int steps = (L + kBN - 1) / kBN;
+        T = L == 0 ? 0 : (pp.split_steps > 0 ? (steps + pp.split_steps - 1) / pp.split_steps : 1);
         return true;
     }
     cq0 = pp.cu_q[b];
@@ -290,9 +300,14 @@ __device__ __forceinline__ int tile_steps(int P, int Lq, int i0, int tq)
     return (P + i0 + min(tq, Lq - i0) + kBN - 1) / kBN;
 }
 
-// A sequence's sort bucket: the key steps of its last listed tile (its heaviest).
-__device__ __forceinline__ int seq_bucket(int P, int Lq, int T, int tq)
+// A sequence's sort bucket: the key steps of its last listed tile (its heaviest); in decode mode
+// the key steps of its first entry.
+__device__ __forceinline__ int seq_bucket(const PlanParams &pp, int P, int Lq, int T, int tq)
 {
+    if (pp.ctx) {
+        const int steps = (P + Lq + kBN - 1) / kBN;
+        return min(pp.split_steps > 0 ? min(steps, pp.split_steps) : steps, kPlanBuckets - 1);
+    }
     return min(tile_steps(P, Lq, (T - 1) * tq, tq), kPlanBuckets - 1);
 }
 
@@ -309,7 +324,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const Pla
     for (int b = tid; b < pp.num_seqs; b += kPlanThreads) {
         int cq0, Lq, P, T;
         if (plan_seq(pp, b, cq0, Lq, P, T) && T > 0)
-            atomicAdd(&hist[seq_bucket(P, Lq, T, pp.tq)], T);
+            atomicAdd(&hist[seq_bucket(pp, P, Lq, T, pp.tq)], T);
     }
     __syncthreads();
     // exclusive prefix sum with the buckets in DESCENDING order: thread tid owns 8 of them
@@ -366,16 +381,23 @@ __global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const Pla
         }
         int first = 0;
         if (lane == 0)
-            first = atomicAdd(&hist[seq_bucket(P, Lq, T, pp.tq)], T);
+            first = atomicAdd(&hist[seq_bucket(pp, P, Lq, T, pp.tq)], T);
         first = __shfl_sync(0xffffffffu, first, 0);
         for (int t = lane; t < T; t += 32) {
-            const int i0 = t * pp.tq;
-            const int nkv = tile_steps(P, Lq, i0, pp.tq);
             const int e = first + (T - 1 - t);
-            if (e < pp.cap) {
+            if (e >= pp.cap)
+                continue;
+            rec[2 * e] = make_int4(b, cq0, Lq, P);
+            if (pp.ctx && pp.split_steps > 0) {
+                // decode split t: key steps n0 .. n0+nkv-1, packed as nkv | n0 << 16
+                const int steps = (P + Lq + kBN - 1) / kBN;
+                const int n0 = t * pp.split_steps;
+                const int nkv = min(pp.split_steps, steps - n0);
+                rec[2 * e + 1] = make_int4(0, 1, P + Lq, nkv | (n0 << 16));
+            } else {
+                const int i0 = t * pp.tq;
                 const int nq = min(pp.tq, Lq - i0);
-                rec[2 * e] = make_int4(b, cq0, Lq, P);
-                rec[2 * e + 1] = make_int4(i0, nq, P + i0 + nq, nkv);
+                rec[2 * e + 1] = make_int4(i0, nq, P + i0 + nq, tile_steps(P, Lq, i0, pp.tq));
             }
         }
     }
@@ -447,6 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         it.kv_len = q[8];
         it.nkv = q[9];
         it.first_masked = q[10];
+        it.n0 = q[11];
         __syncwarp();
         if (lane == 0)
             mbar_arrive(BAR(kBarItemEmpty + k % kQueue));
@@ -499,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld64(s_addr + 64, u1);
                 tmem_wait_ld();
                 float s0[64], s1[64];
-                const int rel = lim - n * kBN;          // keys j <= rel of this tile are visible
+                const int rel = lim - (it.n0 + n) * kBN;   // keys j <= rel of this tile are visible
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
                     s0[j] = (!kMasked || j <= rel) ? __uint_as_float(u0[j]) : -INFINITY;
@@ -545,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             for (int n = 0; n < it.nkv && ok; ++n, ++g)
-                ok = n < it.first_masked ? tile(n, std::false_type{}) : tile(n, std::true_type{});
+                ok = it.n0 + n < it.first_masked ? tile(n, std::false_type{}) : tile(n, std::true_type{});
             if (!ok)
                 break;
             // Hand the row sums to the epilogue warps and go on with the next item at once.  The
@@ -555,6 +578,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             rowsum[(k & 1) * 128 + r] = l_run;
+            if (p.split_steps > 0 && it.kv_len > p.split_steps * kBN && tok < it.Lq) {
+                // a decode split: the row's (max, sum) go straight to the partials (O follows from
+                // the epilogue)
+                const size_t unit = (size_t)it.b * p.max_splits + it.n0 / p.split_steps;
+                const int head = it.kvh * p.group + (r & (p.group - 1));
+                *reinterpret_cast<float2 *>(p.part_ml + (unit * p.num_q_heads + head) * 2) = make_float2(m_run, l_run);
+            }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(BAR(kBarRowSum + (k & 1)));
@@ -568,13 +598,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bs_mask = (1 << p.block_shift) - 1;
         const int boxes = kBN / p.box_rows;
         auto box_slot = [&](const Item &it, int n, const int32_t *bt, int nblk, int &win_base, int &win) {
-            const int lb0 = (n * kBN) >> p.block_shift;
+            const int lb0 = ((it.n0 + n) * kBN) >> p.block_shift;
             const int lb_hi = min(lb0 + boxes - 1, nblk - 1);
             if (lb_hi >= win_base + 32) {               // warp-uniform window move
                 win_base = lb0;
                 win = win_base + lane < nblk ? __ldg(bt + win_base + lane) : -1;
             }
-            const int j0 = n * kBN + lane * p.box_rows;
+            const int j0 = (it.n0 + n) * kBN + lane * p.box_rows;
             const int lb = j0 >> p.block_shift;
             const int blk = __shfl_sync(0xffffffffu, win, (lb - win_base) & 31);
             int slot = -1;
@@ -654,6 +684,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     it.nq = __shfl_sync(0xffffffffu, r.y, 1);
                     it.kv_len = __shfl_sync(0xffffffffu, r.z, 1);
                     it.nkv = __shfl_sync(0xffffffffu, r.w, 1);
+                    it.n0 = 0;
+                    if (p.split_steps > 0) {        // decode split: nkv | n0 << 16
+                        it.n0 = it.nkv >> 16;
+                        it.nkv &= 0xFFFF;
+                    }
                     it.kvh = v - e * p.num_kv_heads;
                     it.first_masked = (it.P + it.i0 + 1) / kBN;
                 }
@@ -670,6 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     q[8] = it.kv_len;
                     q[9] = it.nkv;
                     q[10] = it.first_masked;
+                    q[11] = it.n0;
                     mbar_arrive(BAR(kBarItemFull + k % kQueue));
                 }
                 if (v >= total)
@@ -812,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Keys past the sequence carry P = 0, but their V rows may hold anything (NaN patterns
                 // included) and 0 * NaN would poison O: zero them.  (Skipping their k-steps instead
                 // measured slower.)
-                const int vrows = min(c.it.kv_len - n * kBN, kBN);
+                const int vrows = min(c.it.kv_len - (c.it.n0 + n) * kBN, kBN);
                 if (vrows < kBN) {
                     for (int c2 = lane; c2 < (kBN - vrows) * 16; c2 += 32)     // 16-byte chunk: row, half, column
                         sts_u4(vtile + ((c2 >> 3) & 1) * kHalf + (uint32_t)(vrows + (c2 >> 4)) * 128u +
@@ -882,6 +918,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int head = it.kvh * p.group + (r & (p.group - 1));
                 const bool valid = tok < it.Lq;
                 const float l_row = rowsum[(k & 1) * 128 + r];
+                if (p.split_steps > 0 && it.kv_len > p.split_steps * kBN) {
+                    // a decode split: unnormalised O goes to the partials (the softmax wrote the row's
+                    // max and sum)
+                    const size_t unit = (size_t)it.b * p.max_splits + it.n0 / p.split_steps;
+                    float *po = p.part_o + (unit * p.num_q_heads + head) * kD;
+#pragma unroll
+                    for (int c = 0; c < kD / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(o_addr + c * 32, v);
+                        tmem_wait_ld();
+                        if (valid) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                reinterpret_cast<float4 *>(po + c * 32)[j] =
+                                    make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                        }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(BAR(kBarOFree + (k & 1)));   // O and this item's row sums are read
+                        mbar_arrive(BAR(kBarQEmpty + k % kQBufs));   // its Q buffer was not used for staging
+                    }
+                    continue;
+                }
                 const float inv = (valid && l_row > 0.f) ? 1.f / l_row : 0.f;
                 // O -> registers as bf16 pairs, 32 columns at a time
                 uint32_t ob[kD / 2];
@@ -1030,7 +1092,12 @@ int nvkv_host::tile_attention(const TileAttnArgs &a)
         return NV_ERR_ALIGN;
     if (num_blocks == 0)
         return NV_ERR_SHAPE;
-    const int64_t cap = prefill_entries_cap(num_seqs, total_q, max_seqlen_q, group);
+    const bool split = a.context_lens && a.split_steps > 0;
+    if (split && (a.split_steps >= (1 << 16) || (int64_t)a.max_splits * a.split_steps >= (1 << 15) ||
+                  !a.part_o || !a.part_ml))
+        return NV_ERR_UNSUPPORTED;    // an entry packs its step count and first step in 16 bits each
+    const int64_t cap = split ? (int64_t)num_seqs * a.max_splits
+                              : prefill_entries_cap(num_seqs, total_q, max_seqlen_q, group);
     if (cap * num_kv_heads >= (1ll << 31))
         return NV_ERR_UNSUPPORTED;
     if (!a.workspace || a.workspace_bytes < prefill_workspace_bytes(cap) || !aligned16(a.workspace))
@@ -1060,6 +1127,10 @@ int nvkv_host::tile_attention(const TileAttnArgs &a)
     p.num_kv_heads = num_kv_heads;
     p.scale_log2 = a.scale * nvkv::kLog2e;
     p.ws = static_cast<int32_t *>(a.workspace);
+    p.split_steps = split ? a.split_steps : 0;
+    p.max_splits = split ? a.max_splits : 0;
+    p.part_o = a.part_o;
+    p.part_ml = a.part_ml;
 
     PlanParams pp{};
     pp.cu_q = a.cu_seqlens_q;
@@ -1077,6 +1148,7 @@ int nvkv_host::tile_attention(const TileAttnArgs &a)
     pp.cap = (int32_t)cap;
     pp.max_len = a.max_len;
     pp.row_u4 = num_q_heads * kD / 8;
+    pp.split_steps = p.split_steps;
     const int sms = sm_count();
     if (sms <= 0)
         return NV_ERR_CUDA;

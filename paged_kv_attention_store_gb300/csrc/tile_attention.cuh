@@ -27,6 +27,11 @@ struct TileAttnArgs {
     int32_t block_size;
     int32_t num_blocks;
     int32_t max_len;                  // decode mode: contexts longer than this are truncated to it
+    int32_t split_steps;              // decode mode: 128-key steps per split (0: no split); a sequence
+                                      // with more writes fp32 partials for a merge launch
+    int32_t max_splits;               // splits of the longest sequence
+    float *part_o;                    // [num_seqs, max_splits, num_q_heads, 128]
+    float *part_ml;                   // [num_seqs, max_splits, num_q_heads, 2]: log2-domain max, sum
     float scale;
     void *out;
     void *workspace;

@@ -93,12 +93,13 @@ def test_decode_validation(lib):
 
 
 def test_decode_workspace_size_follows_the_split_rule(lib):
-    """256 KiB of split counters, then num_seqs x splits x Hq x (128 + 2) floats of partials; the
-    split is 512 positions halved while the batch has fewer than 1200 units, stopping at 256 once
-    it has 600 (and at 64 at the least)."""
+    """256 KiB of split counters, then num_seqs x splits x Hq x (128 + 2) floats of partials, then a
+    tile-kernel work list of 64 bytes + 32 per (sequence, split); the split is 512 positions halved
+    while the batch has fewer than 1200 units, stopping at 256 once it has 600 (and at 64 at the
+    least)."""
     def size(B, L, hq=32):
         return lib.nv_paged_decode_workspace_size(B, hq, 128, L)
-    part = lambda B, splits, hq=32: 256 * 1024 + B * splits * hq * 130 * 4
+    part = lambda B, splits, hq=32: 256 * 1024 + B * splits * hq * 130 * 4 + 64 + 32 * B * splits
     assert size(512, 4096) == part(512, 8)        # 4096 units at 512 positions
     assert size(256, 2048, 16) == part(256, 8, 16)  # 1024 units at 512 -> 2048 at 256
     assert size(64, 4096) == part(64, 16)         # 512 -> 1024 units at 256: stop (>= 600)

@@ -237,3 +237,11 @@ def test_decode_group8_bad_block_id_is_flagged_not_faulted():
     # the same in both)
     want = oracle_decode(oracle.default(), b, db.kc_host0, db.vc_host0)
     compare(got[1:2], want[1:2], "unaffected row")
+
+
+def test_decode_group8_one_long_sequence_splits_its_keys():
+    """One sequence of 20000 keys at group 8 gives the tile kernel 8 (sequence, kv head) units; its keys
+    are split into ranges of 1024 whose fp32 partials a merge launch combines."""
+    b = W.make_decode("g8-one", 33, [20000], 64, 8, 128, 256)
+    db, got, kc, vc = _run(b)
+    compare(got, oracle_decode(oracle.default(), b, kc, vc), b.name)

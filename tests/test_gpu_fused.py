@@ -47,7 +47,8 @@ CASES = [
     ("g1-bs16", [1, 8, 9, 16, 17, 333], 8, 8, 16, 2),
     ("g8-bs32", [10, 32, 33, 900], 16, 2, 32, 1),
     ("g2-hkv16", [2, 40, 513], 32, 16, 16, 0),
-    ("g8-hkv8", [1, 257, 1100, 3000], 64, 8, 256, 1),   # one of the two warps per kv head stores
+    ("g8-hkv8", [1, 257, 1100, 3000], 64, 8, 256, 1),   # store pass + tile kernel, keys split
+    ("g8-long", [5, 9000], 64, 8, 64, 0),
     ("g4-hkv12", [4, 129, 700], 48, 12, 32, 0),
 ]
 

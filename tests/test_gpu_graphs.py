@@ -92,17 +92,19 @@ class _Static:
         return host_bits(self.k_cache[:b.num_blocks]), host_bits(self.v_cache[:b.num_blocks])
 
 
+@pytest.mark.parametrize("hq", [32, 64], ids=["group4", "group8-tiles"])
 @pytest.mark.parametrize("fused", [False, True], ids=["store+decode", "fused"])
-def test_decode_step_replayed_from_a_graph(fused):
-    """A 16-row decode bucket: one batch fills it, the other has 12 real rows and 4 padding rows."""
+def test_decode_step_replayed_from_a_graph(fused, hq):
+    """A 16-row decode bucket: one batch fills it, the other has 12 real rows and 4 padding rows.  At
+    group 8 the step runs the tile kernel with the keys split and a merge launch."""
     import torch
     orc = oracle.default()
     rng = np.random.default_rng(71)
-    full = W.make_decode("graph-full", 71, rng.integers(1, 3000, 16).tolist(), 32, 8, 128, 64, width=48)
-    padded = W.make_decode("graph-pad", 72, rng.integers(1, 3000, 12).tolist(), 32, 8, 128, 64, n_pad=4, width=48)
+    full = W.make_decode("graph-full", 71, rng.integers(1, 3000, 16).tolist(), hq, 8, 128, 64, width=48)
+    padded = W.make_decode("graph-pad", 72, rng.integers(1, 3000, 12).tolist(), hq, 8, 128, 64, n_pad=4, width=48)
     st = _Static([full, padded], rows=16)
     max_ctx = st.width * full.block_size
-    ws = torch.zeros(nv.nv_paged_decode_workspace_size(16, 32, 128, max_ctx), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(nv.nv_paged_decode_workspace_size(16, hq, 128, max_ctx), dtype=torch.uint8, device="cuda")
 
     def step():
         if fused:
