@@ -409,6 +409,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const Pla
     }
 }
 
+// kRanges: work items may cover a range of key steps and write decode partials (the decode split);
+// prefill runs the instantiation without, so none of it costs the prefill softmax anything.
+template <bool kRanges>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
@@ -475,6 +478,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(BAR(kBarItemEmpty + k % kQueue));
         return true;
     };
+    auto first_step = [](const Item &x) {           // an item's first key step (0 without ranges)
+        if constexpr (kRanges)
+            return x.n0;
+        else
+            return 0;
+    };
     if (warp == kWarpS) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
@@ -522,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld64(s_addr + 64, u1);
                 tmem_wait_ld();
                 float s0[64], s1[64];
-                const int rel = lim - (it.n0 + n) * kBN;   // keys j <= rel of this tile are visible
+                const int rel = lim - (first_step(it) + n) * kBN;   // keys j <= rel of this tile are visible
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
                     s0[j] = (!kMasked || j <= rel) ? __uint_as_float(u0[j]) : -INFINITY;
@@ -568,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             for (int n = 0; n < it.nkv && ok; ++n, ++g)
-                ok = it.n0 + n < it.first_masked ? tile(n, std::false_type{}) : tile(n, std::true_type{});
+                ok = first_step(it) + n < it.first_masked ? tile(n, std::false_type{}) : tile(n, std::true_type{});
             if (!ok)
                 break;
             // Hand the row sums to the epilogue warps and go on with the next item at once.  The
@@ -578,12 +587,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             rowsum[(k & 1) * 128 + r] = l_run;
-            if (p.split_steps > 0 && it.kv_len > p.split_steps * kBN && tok < it.Lq) {
-                // a decode split: the row's (max, sum) go straight to the partials (O follows from
-                // the epilogue)
-                const size_t unit = (size_t)it.b * p.max_splits + it.n0 / p.split_steps;
-                const int head = it.kvh * p.group + (r & (p.group - 1));
-                *reinterpret_cast<float2 *>(p.part_ml + (unit * p.num_q_heads + head) * 2) = make_float2(m_run, l_run);
+            if constexpr (kRanges) {
+                if (it.kv_len > p.split_steps * kBN && tok < it.Lq) {
+                    // a decode split: the row's (max, sum) go straight to the partials (O follows from
+                    // the epilogue)
+                    const size_t unit = (size_t)it.b * p.max_splits + it.n0 / p.split_steps;
+                    const int head = it.kvh * p.group + (r & (p.group - 1));
+                    *reinterpret_cast<float2 *>(p.part_ml + (unit * p.num_q_heads + head) * 2) =
+                        make_float2(m_run, l_run);
+                }
             }
             __syncwarp();
             if (lane == 0)
@@ -598,13 +610,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bs_mask = (1 << p.block_shift) - 1;
         const int boxes = kBN / p.box_rows;
         auto box_slot = [&](const Item &it, int n, const int32_t *bt, int nblk, int &win_base, int &win) {
-            const int lb0 = ((it.n0 + n) * kBN) >> p.block_shift;
+            const int lb0 = ((first_step(it) + n) * kBN) >> p.block_shift;
             const int lb_hi = min(lb0 + boxes - 1, nblk - 1);
             if (lb_hi >= win_base + 32) {               // warp-uniform window move
                 win_base = lb0;
                 win = win_base + lane < nblk ? __ldg(bt + win_base + lane) : -1;
             }
-            const int j0 = (it.n0 + n) * kBN + lane * p.box_rows;
+            const int j0 = (first_step(it) + n) * kBN + lane * p.box_rows;
             const int lb = j0 >> p.block_shift;
             const int blk = __shfl_sync(0xffffffffu, win, (lb - win_base) & 31);
             int slot = -1;
@@ -685,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     it.kv_len = __shfl_sync(0xffffffffu, r.z, 1);
                     it.nkv = __shfl_sync(0xffffffffu, r.w, 1);
                     it.n0 = 0;
-                    if (p.split_steps > 0) {        // decode split: nkv | n0 << 16
+                    if constexpr (kRanges) {        // decode split: nkv | n0 << 16
                         it.n0 = it.nkv >> 16;
                         it.nkv &= 0xFFFF;
                     }
@@ -848,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Keys past the sequence carry P = 0, but their V rows may hold anything (NaN patterns
                 // included) and 0 * NaN would poison O: zero them.  (Skipping their k-steps instead
                 // measured slower.)
-                const int vrows = min(c.it.kv_len - (c.it.n0 + n) * kBN, kBN);
+                const int vrows = min(c.it.kv_len - (first_step(c.it) + n) * kBN, kBN);
                 if (vrows < kBN) {
                     for (int c2 = lane; c2 < (kBN - vrows) * 16; c2 += 32)     // 16-byte chunk: row, half, column
                         sts_u4(vtile + ((c2 >> 3) & 1) * kHalf + (uint32_t)(vrows + (c2 >> 4)) * 128u +
@@ -918,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int head = it.kvh * p.group + (r & (p.group - 1));
                 const bool valid = tok < it.Lq;
                 const float l_row = rowsum[(k & 1) * 128 + r];
-                if (p.split_steps > 0 && it.kv_len > p.split_steps * kBN) {
+                if (kRanges && it.kv_len > p.split_steps * kBN) {
                     // a decode split: unnormalised O goes to the partials (the softmax wrote the row's
                     // max and sum)
                     const size_t unit = (size_t)it.b * p.max_splits + it.n0 / p.split_steps;
@@ -1156,14 +1168,18 @@ int nvkv_host::tile_attention(const TileAttnArgs &a)
     static cudaError_t attr_err = cudaSuccess;
     static bool regs_ok = false;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(paged_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         // the warpgroups' register split (setmaxnreg) adds up to exactly the launch budget: refuse to
         // launch a build whose per-thread register count differs, rather than let a warpgroup wait
         // for registers that never come
-        cudaFuncAttributes fa{};
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncGetAttributes(&fa, paged_prefill_kernel);
-        regs_ok = attr_err == cudaSuccess && fa.numRegs == kLaunchRegs;
+        regs_ok = true;
+        for (const void *f : {(const void *)paged_prefill_kernel<false>, (const void *)paged_prefill_kernel<true>}) {
+            if (attr_err == cudaSuccess)
+                attr_err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            cudaFuncAttributes fa{};
+            if (attr_err == cudaSuccess)
+                attr_err = cudaFuncGetAttributes(&fa, f);
+            regs_ok = regs_ok && attr_err == cudaSuccess && fa.numRegs == kLaunchRegs;
+        }
     });
     if (attr_err != cudaSuccess)
         return NV_ERR_CUDA;
@@ -1186,7 +1202,9 @@ int nvkv_host::tile_attention(const TileAttnArgs &a)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, paged_prefill_kernel, tq_map, tk, tv, to, p) != cudaSuccess)
+    const cudaError_t le = split ? cudaLaunchKernelEx(&cfg, paged_prefill_kernel<true>, tq_map, tk, tv, to, p)
+                                 : cudaLaunchKernelEx(&cfg, paged_prefill_kernel<false>, tq_map, tk, tv, to, p);
+    if (le != cudaSuccess)
         return NV_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? NV_OK : NV_ERR_CUDA;
 }
