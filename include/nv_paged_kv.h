@@ -261,9 +261,9 @@ int nv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache
  *                 (NV_DERR_SLOT_RANGE when it lies outside the pool).
  * The result (cache and out) equals nv_store_kvcache then nv_paged_decode_attn with the same
  * arguments whenever the slots follow that rule.  Groups 8 and 16 (which decode on the tile kernel)
- * apply the same rule in a separate store pass before the decode's two launches.  The new slots must not lie in another
- * sequence's history within the same call (they never do: a new token's slot belongs to its
- * own sequence).
+ * apply the same rule in a separate store pass before the decode's launches.  The new slots must
+ * not lie in another sequence's history within the same call (they never do: a new token's slot
+ * belongs to its own sequence).
  */
 int nv_store_decode_attn(const void *q, const void *k, int64_t k_row_stride, const void *v, int64_t v_row_stride,
                          const int32_t *slot_mapping, void *k_cache, void *v_cache, const int32_t *block_tables,

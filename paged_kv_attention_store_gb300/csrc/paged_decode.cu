@@ -26,8 +26,9 @@
 //   * HBM-bound (about 4 flop per byte of KV), so no tensor cores: fp32 FMAs on CUDA cores.
 //   * A sequence split over several CTAs writes unnormalised partial outputs plus its
 //     (max, sum); the sequence's last CTA to finish (a per-sequence counter in the workspace)
-//     combines them and writes the bf16 output, so no separate merge pass runs.  Single-split
-//     sequences write bf16 output directly.
+//     combines them and writes the bf16 output, so no separate merge pass runs -- except above
+//     16 splits (small batches of long contexts), where merge_splits_kernel follows with a CTA
+//     per (sequence, query head).  Single-split sequences write bf16 output directly.
 //   * nv_store_decode_attn (the store of the same forward fused in; kFused): the CTA whose
 //     split holds position L-1 copies the new K/V row from the inputs into its last staged
 //     chunk instead of from the pool, and its consumer warps write that row to its slot.
