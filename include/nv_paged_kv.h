@@ -283,7 +283,8 @@ int nv_store_decode_attn(const void *q, const void *k, int64_t k_row_stride, con
  * which every GPU that loads the library holds until the process exits.
  *
  * Arguments and results are those of nv_paged_decode_attn (same kernels; groups 8 and 16 keep the
- * tile kernel's work list in the same static array).  The split length
+ * tile kernel's work list, and its split partials when a batch's keys are split, in the same static
+ * array, and do not split when they would not fit).  The split length
  * is the usual one, doubled (up to 4096 positions) while the partials would not fit the
  * array; a batch whose partials still exceed it (num_seqs * splits * num_q_heads * 520 bytes)
  * is rejected with NV_ERR_WORKSPACE before anything is enqueued.
