@@ -25,6 +25,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -459,7 +460,10 @@ def run_ours(args, rank, world, local_rank):
             if ev is not None:
                 ev[2].record(stream)
 
-        for _ in range(args.warmup):
+        # the warm-up runs the flush too: the first call of its kernels (lazily loaded by the runtime)
+        # stalled the host for ~60 us inside the first timed step, which then measured 84 us
+        for i in range(args.warmup):
+            flush_l2(i)
             prefill_step()
         barrier()
         pev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
@@ -482,7 +486,8 @@ def run_ours(args, rank, world, local_rank):
             nv.nv_qk_norm_rope_store(pqkv, ppos, pqw, pkw, pslots, pk_cache, pv_cache, pb.num_q_heads,
                                      rms_eps=pi.eps, rope_theta=pi.theta, q_out=pq_out, d_err=d_err)
 
-        for _ in range(args.warmup):
+        for i in range(args.warmup):
+            flush_l2(i)
             prologue_step()
         barrier()
         rev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(2)) for _ in range(args.steps)]
@@ -682,6 +687,30 @@ def output_error(got_bits: np.ndarray, want: np.ndarray) -> dict:
             "rel_l2": float(np.linalg.norm(got - want) / max(float(np.linalg.norm(want)), 1e-30))}
 
 
+def host_cpu() -> dict:
+    """The host the CPU legs run on: its core count and CPU model (``lscpu``'s model name where
+    /proc/cpuinfo has none, as on Arm hosts)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if not model:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.strip().lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    return {"host_cores": os.cpu_count(), "cpu_model": model or platform.machine()}
+
+
 def cpu_baseline_decode(b: W.PagedBatch, seconds: float, max_seqs: int | None = None, collect: dict | None = None):
     """Oracle decode, single thread, sequence by sequence until ~`seconds` of CPU work (outputs into
     `collect`, by sequence, when given)."""
@@ -704,7 +733,7 @@ def cpu_baseline_decode(b: W.PagedBatch, seconds: float, max_seqs: int | None = 
         if spent >= seconds or (max_seqs and done >= max_seqs):
             break
     kv = tokens * b.num_kv_heads * KV_BYTES_PER_TOKEN_PER_KVHEAD
-    return {"value": round(kv / spent / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": round(kv / spent / 1e9, 4), "unit": "GB/s", "cores": 1, **host_cpu(), "kind": "oracle",
             "sample": f"{done} of {b.num_seqs} sequences ({tokens} attended positions x {b.num_q_heads} heads) "
                       f"of the same decode batch, one thread, {spent:.1f} s",
             "seconds": round(spent, 2), "attended_tok_s": round(tokens / spent, 1)}
@@ -736,7 +765,7 @@ def cpu_baseline_prefill(b: W.PagedBatch, seconds: float, collect: dict | None =
             pairs += int(P[s]) + int(r - cu[s]) + 1
         done += chunk.size
     flops = 4 * 128 * b.num_q_heads * pairs
-    return {"value": round(flops / spent / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+    return {"value": round(flops / spent / 1e12, 6), "unit": "TFLOP/s", "cores": 1, **host_cpu(), "kind": "oracle",
             "sample": f"{done} of {int(b.q_lens.sum())} query rows ({pairs} causal pairs x {b.num_q_heads} heads) "
                       f"of the same prefill batch, one thread, {spent:.1f} s",
             "seconds": round(spent, 2)}
@@ -769,7 +798,7 @@ def run_reference(args, rank, world):
         "data": "synthetic: seeded N(0,1) values rounded to bf16, block tables dealt from a shuffled pool",
         "config": {"workload": "qwen3-8b-shaped decode step (store + paged decode), "
                                f"{per_step} sampled sequence(s) per step", "num_seqs": db.num_seqs},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, **host_cpu(), "kind": "oracle",
                          "sample": f"{per_step} sequence(s) of the 512-sequence batch per step, one thread"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "wall_s": round(wall, 2),

@@ -22,8 +22,13 @@
  *     in logical order, padded with -1 (Step 07.7).  Entries beyond the blocks a sequence's
  *     length needs are never read.
  *   - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
- *   - head_dim must be 128; block_size a power of two in [16, 256]; num_q_heads a multiple of
- *     num_kv_heads with a group of at most 8 (decode) / 16 (prefill); num_kv_heads <= 16.
+ *   - Shape limits, the same for decode and prefill unless an entry point adds its own:
+ *     head_dim must be 128 and block_size a power of two in [16, 256] (else NV_ERR_UNSUPPORTED);
+ *     num_q_heads a multiple of num_kv_heads (else NV_ERR_SHAPE), with a group
+ *     G = num_q_heads / num_kv_heads of 1, 2, 4, 8 or 16 (else NV_ERR_UNSUPPORTED).  Decode takes
+ *     num_kv_heads <= 16 and a pool of fewer than 2^40 values per tensor (num_blocks * block_size *
+ *     num_kv_heads * head_dim); prefill, and decode at G = 8 or 16, take num_seqs <= 65535 and
+ *     num_blocks * block_size < 2^31 (else NV_ERR_UNSUPPORTED).
  *   - Host-side argument errors return a negative nv_status before anything is enqueued.
  *     Data-dependent errors found on the device (a slot or block id outside the pool, a
  *     length beyond what the block table or the host hint allows) never fault: the offending

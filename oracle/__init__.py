@@ -264,21 +264,35 @@ def qk_norm_rope_store(*args, **kw):
 
 
 def _parallel(run, n, threads):
+    """Run ``run(lo, hi)`` over [0, n) on ``threads`` Python threads (the C routines release the GIL).
+
+    The range is cut into about eight pieces per thread, handed out in order as threads come free,
+    so a few expensive rows (long contexts) do not leave the other threads idle."""
     threads = max(1, min(int(threads), n))
     if threads == 1:
         if n:
             run(0, n)
         return
-    bounds = np.linspace(0, n, threads + 1).astype(int)
+    pieces = min(n, threads * 8)
+    bounds = np.linspace(0, n, pieces + 1).astype(int)
+    nxt = [0]
+    lock = threading.Lock()
     errors = []
 
-    def guarded(lo, hi):
-        try:
-            run(lo, hi)
-        except BaseException as e:  # re-raised on the calling thread below
-            errors.append(e)
+    def worker():
+        while True:
+            with lock:
+                i = nxt[0]
+                nxt[0] += 1
+            if i >= pieces or errors:
+                return
+            try:
+                run(int(bounds[i]), int(bounds[i + 1]))
+            except BaseException as e:  # re-raised on the calling thread below
+                errors.append(e)
+                return
 
-    ts = [threading.Thread(target=guarded, args=(int(bounds[i]), int(bounds[i + 1]))) for i in range(threads)]
+    ts = [threading.Thread(target=worker) for _ in range(threads)]
     for t in ts:
         t.start()
     for t in ts:

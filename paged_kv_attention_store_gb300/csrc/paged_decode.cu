@@ -32,6 +32,7 @@
 //   * nv_store_decode_attn (the store of the same forward fused in; kFused): the CTA whose
 //     split holds position L-1 copies the new K/V row from the inputs into its last staged
 //     chunk instead of from the pool, and its consumer warps write that row to its slot.
+#include <atomic>
 #include <mutex>
 
 #include "nv_common.cuh"
@@ -619,12 +620,16 @@ template <int G, int MAXH, bool kFused>
 int launch_decode(const DecodeParams &p, int num_seqs, cudaStream_t stream)
 {
     const size_t smem_bytes = decode_smem_bytes(kStages, p.num_kv_heads);
-    static bool configured = false;   // benign race: every thread sets the same attribute value
-    if (!configured) {
+    // The shared-memory opt-in is a per-device attribute: bit d records that device d has it.
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return NV_ERR_CUDA;
+    if (!((configured.load(std::memory_order_acquire) >> dev) & 1u)) {
         if (cudaFuncSetAttribute(paged_decode_kernel<G, MAXH, kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem_bytes > 200 * 1024 ? 227 * 1024 : 200 * 1024) != cudaSuccess)
             return NV_ERR_CUDA;
-        configured = true;
+        configured.fetch_or(1ull << dev, std::memory_order_release);
     }
     dim3 grid(num_seqs, p.max_splits);
     paged_decode_kernel<G, MAXH, kFused><<<grid, (p.num_kv_heads + 1) * 32, smem_bytes, stream>>>(p);
@@ -669,6 +674,13 @@ int run_split_kv(int group, DecodeParams &p, int num_seqs, cudaStream_t st)
 // byte and stop keeping up with HBM at G = 8 (measured 0.54 of the HBM roofline there, against
 // about 1.0 for the tile kernel on the same batch).  Its work list sits after the split counters.
 constexpr int kTileGroup = 8;
+
+// The tile kernel's own limits (its work list packs sequence ids and pool slots in 16 and 31 bits),
+// checked before the workspace so the refusal does not depend on it.
+bool tile_shape_ok(int32_t num_seqs, int32_t num_blocks, int32_t block_size)
+{
+    return num_seqs <= 65535 && (int64_t)num_blocks * block_size < (1ll << 31);
+}
 
 size_t tile_list_bytes(int32_t num_seqs)
 {
@@ -858,6 +870,8 @@ int decode_entry(const void *q, const void *k_cache, const void *v_cache, const 
         p.num_slots = (int64_t)num_blocks * block_size;
     }
     if (group >= kTileGroup) {
+        if (!tile_shape_ok(num_seqs, num_blocks, block_size))
+            return NV_ERR_UNSUPPORTED;
         if (!workspace || workspace_bytes < kCounterBytes + tile_list_bytes(num_seqs) || !aligned16(workspace))
             return NV_ERR_WORKSPACE;
         if (st) {       // the store first, by the fused kernel's rule; then the decode reads the pool
@@ -986,6 +1000,8 @@ extern "C" int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, 
     const int64_t bt_cap = (int64_t)bt_stride * block_size;
     const int max_len = (int)(bt_cap < max_context_len ? bt_cap : max_context_len);
     if (group >= kTileGroup) {     // the tile kernel's work list goes in the static array
+        if (!tile_shape_ok(num_seqs, num_blocks, block_size))
+            return NV_ERR_UNSUPPORTED;
         void *scratch = nullptr;
         int32_t *counters = nullptr;
         if (!static_arrays(&scratch, &counters))

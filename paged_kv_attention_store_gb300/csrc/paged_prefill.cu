@@ -55,11 +55,8 @@ constexpr int kD = 128;
 constexpr int kBM = 128;             // rows per query tile (TMEM lanes)
 constexpr int kBN = 128;             // keys per K/V tile
 constexpr int kQBufs = 2;            // Q buffers: the next item's Q loads while this one runs
-#ifndef NVKV_PREFILL_KSLOTS
-#define NVKV_PREFILL_KSLOTS 3
-#endif
-constexpr int kKSlots = NVKV_PREFILL_KSLOTS;   // K ring slots
-constexpr int kVSlots = 5 - kKSlots;           // V ring slots
+constexpr int kKSlots = 3;           // K ring slots
+constexpr int kVSlots = 2;           // V ring slots
 constexpr int kBufs = 3;             // score / P buffers in TMEM
 // Warp roles: 0-3 softmax (warpgroup 0); 4 TMA producer of Q and K; 5 S = Q K^T issuer (owns TMEM);
 // 6 O += P V issuer; 7-10 epilogue (TMEM lane quarter = warp % 4); 11 TMA producer of V.  Warpgroup 0 runs with more
@@ -72,12 +69,6 @@ static_assert(4 * kSoftmaxRegs + 8 * kOtherRegs == 12 * kLaunchRegs, "register s
 constexpr uint32_t kTmemCols = 512;  // buffer b at b*128, O at 384
 constexpr uint32_t kTmemO = 384;
 constexpr float kRescaleLog2 = 8.0f;
-// Of every 8 score pairs, this many take the polynomial exp2 on the FMA pipe; the rest use the
-// special-function unit.
-#ifndef NVKV_PREFILL_POLY_PAIRS
-#define NVKV_PREFILL_POLY_PAIRS 0
-#endif
-constexpr int kPolyPairs = NVKV_PREFILL_POLY_PAIRS;
 
 constexpr uint32_t kHalf = 128 * 128;         // 128 rows x 64 dims bf16 (one swizzle atom wide) = 16 KB
 constexpr uint32_t kTile = 2 * kHalf;         // a 128 x 128 bf16 operand = 32 KB
@@ -99,7 +90,8 @@ constexpr int kBarRowSum = kBarOFree + 2;          // + item parity: the softmax
 constexpr int kBarItemFull = kBarRowSum + 2;       // + queue slot
 constexpr int kBarItemEmpty = kBarItemFull + kQueue;
 constexpr int kItemReaders = 2 + 4 + 4 + 1;        // S cursor, PV cursor, 4 softmax, 4 epilogue warps, V copies
-constexpr int kNumBars = kBarItemEmpty + kQueue;
+constexpr int kBarDrain = kBarItemEmpty + kQueue;   // + issuer warp: its last MMAs, after a wait gave up
+constexpr int kNumBars = kBarDrain + 2;
 constexpr uint32_t kOffItems = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffRowSum = kOffItems + kQueue * kItemInts * 4;   // float [2 item parities][128 rows]
 constexpr uint32_t kOffTmemSlot = kOffRowSum + 2 * 128 * 4;
@@ -159,31 +151,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c)
     return d;
 }
 
-// 2^x0, 2^x1 on the FMA pipe (packed fp32x2), for x <= 8 (scores minus a running max).
-// Range reduction: adding 1.5 * 2^23 rounds x to the nearest integer j, held in the low
-// mantissa bits of the sum; f = x - j lies in [-0.5, 0.5] and 2^f comes from a cubic fitted to
-// minimise the relative error on that interval (max relative error 7.6e-5, well below the bf16
-// rounding of P); finally j is added into the exponent field.  x is clamped at -126 so masked
-// scores (-inf) give a normal number of order 1e-38 instead of a wrapped exponent.
-__device__ __forceinline__ void exp2_poly3_x2(float x0, float x1, float &p0, float &p1)
-{
-    constexpr float kC0 = 0.9999282882344301f, kC1 = 0.6932609081979648f;
-    constexpr float kC2 = 0.24260776842531798f, kC3 = 0.05517030853684025f;
-    constexpr float kRound = 12582912.0f;
-    const uint64_t x = f2_pack(fmaxf(x0, -126.0f), fmaxf(x1, -126.0f));
-    const uint64_t y = f2_add(x, f2_pack(kRound, kRound));
-    const uint64_t j = f2_add(y, f2_pack(-kRound, -kRound));
-    const uint64_t f = f2_fma(j, f2_pack(-1.0f, -1.0f), x);
-    uint64_t q = f2_fma(f2_pack(kC3, kC3), f, f2_pack(kC2, kC2));
-    q = f2_fma(q, f, f2_pack(kC1, kC1));
-    q = f2_fma(q, f, f2_pack(kC0, kC0));
-    float q0, q1, y0, y1;
-    f2_unpack(q, q0, q1);
-    f2_unpack(y, y0, y1);
-    p0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(y0) << 23));
-    p1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(y1) << 23));
-}
-
 // Max of 64 scores with 3-input max (32 instructions, 4 levels deep).
 __device__ __forceinline__ float max64(const float (&s)[64])
 {
@@ -208,14 +175,9 @@ __device__ __forceinline__ float exp_pack64(const float (&s)[64], float scale_lo
     uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
-        float x0, x1, p0, p1;
+        float x0, x1;
         f2_unpack(f2_fma(f2_pack(s[2 * k], s[2 * k + 1]), scale2, negm2), x0, x1);
-        if ((k & 7) >= 8 - kPolyPairs) {
-            exp2_poly3_x2(x0, x1, p0, p1);
-        } else {
-            p0 = fast_exp2(x0);
-            p1 = fast_exp2(x1);
-        }
+        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
         rs2[k & 3] = f2_add(rs2[k & 3], f2_pack(p0, p1));
         pk[k] = pack_bf16x2(p0, p1);
     }
@@ -429,6 +391,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar = base + kOffBar;
     auto BAR = [&](int i) { return bar + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmemSlot);
+    // set by any warp whose bounded wait gave up: the CTA then lets its copies and MMAs land before it
+    // frees tensor memory and leaves
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffTmemSlot + 4);
+    // copies this CTA's producers issued (warp-uniform in the producer warps), for that drain
+    int k_copies = 0, q_copies = 0, v_copies = 0;
+    auto give_up = [&]() {
+        *abort_flag = 1;
+        flag_error(p.d_err, NV_DERR_TIMEOUT);
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
@@ -452,6 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(BAR(kBarItemFull + s), 1);
             mbar_init(BAR(kBarItemEmpty + s), kItemReaders);
         }
+        mbar_init(BAR(kBarDrain), 1);
+        mbar_init(BAR(kBarDrain + 1), 1);
+        *abort_flag = 0;
         fence_barrier_init();
     }
     // Work items pass from the producer (which claims them) to the MMA issuer's two cursors and
@@ -602,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(BAR(kBarRowSum + (k & 1)));
         }
         if (!ok && lane == 0)
-            flag_error(p.d_err, NV_DERR_TIMEOUT);
+            give_up();
     } else {
         warpgroup_reg_dealloc<kOtherRegs>();
         // this lane's box of key tile n of an item (its first pool slot, -1 = none); the block-table
@@ -651,6 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(dst, map, 0, kvh, slot, full);
                 tma_load_3d(dst + kHalf, map, 64, kvh, slot, full);
             }
+            ++(is_v ? v_copies : k_copies);
             return true;
         };
         if (warp == kWarpProducer) {
@@ -742,12 +717,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tma_load_3d(base + kOffQ + qb * kTile + h * kHalf, &tmap_q, h * 64,
                                             it.kvh * p.group, it.cq0 + it.i0, BAR(kBarQFull + qb));
                         }
+                        ++q_copies;
                     }
                     ok = copy_tile(false, j, it.kvh, slot);
                 }
             }
             if (!ok && lane == 0)
-                flag_error(p.d_err, NV_DERR_TIMEOUT);
+                give_up();
         } else if (warp == kWarpVProducer) {
             // ========================= TMA producer: V =========================
             // Copies each item's V tiles into the V ring as soon as the PV issuer frees a slot,
@@ -772,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = copy_tile(true, j, it.kvh, box_slot(it, n, bt, nblk, win_base, win));
             }
             if (!ok && lane == 0)
-                flag_error(p.d_err, NV_DERR_TIMEOUT);
+                give_up();
         } else if (warp == kWarpS || warp == kWarpPV) {
             // ============================ MMA issuer(s) ============================
             // Key steps of all this CTA's work items form one global sequence g.  S(g) goes to TMEM
@@ -895,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     issue_pv(cp);
             }
             if (!ok && lane == 0)
-                flag_error(p.d_err, NV_DERR_TIMEOUT);
+                give_up();
         } else if (warp >= kWarpEpi0 && warp < kWarpEpiEnd) {
             // ============================ epilogue (warps 7-10) ============================
             // Item by item: wait for the softmax's row sums and the item's last PV, read O from TMEM
@@ -1002,13 +978,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(BAR(kBarQEmpty + qb));
             }
             if (!ok && lane == 0)
-                flag_error(p.d_err, NV_DERR_TIMEOUT);
+                give_up();
         }
     }
 
     // ---------------- teardown: every TMEM access is done before the free ----------------
+    // On the normal path every copy and MMA this CTA issued has been waited for by the warp that
+    // consumes it.  After a wait gave up that no longer holds: copies may still be landing in shared
+    // memory and MMAs still reading it and writing tensor memory.  So each producer waits for the
+    // copies it issued last (one per ring slot: all earlier ones were consumed, or their slot reused
+    // after they landed), each issuing thread commits its MMAs to a barrier of its own and waits
+    // for it, and only then is tensor memory freed and the CTA's shared memory released.  Every
+    // wait is bounded as usual.
     tc_fence_before();
     __syncthreads();
+    if (*abort_flag) {
+        if (lane == 0) {
+            if (warp == kWarpProducer) {
+                for (int i = max(0, k_copies - kKSlots); i < k_copies; ++i)
+                    mbar_wait(BAR(kBarKFull + i % kKSlots), (i / kKSlots) & 1);
+                for (int i = max(0, q_copies - kQBufs); i < q_copies; ++i)
+                    mbar_wait(BAR(kBarQFull + i % kQBufs), (i / kQBufs) & 1);
+            } else if (warp == kWarpVProducer) {
+                for (int i = max(0, v_copies - kVSlots); i < v_copies; ++i)
+                    mbar_wait(BAR(kBarVFull + i % kVSlots), (i / kVSlots) & 1);
+            } else if (warp == kWarpS || warp == kWarpPV) {
+                mma_commit(BAR(kBarDrain + (warp - kWarpS)));
+                mbar_wait(BAR(kBarDrain + (warp - kWarpS)), 0);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
     if (warp == kWarpS) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -1164,27 +1165,36 @@ int nvkv_host::tile_attention(const TileAttnArgs &a)
     const int sms = sm_count();
     if (sms <= 0)
         return NV_ERR_CUDA;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    static bool regs_ok = false;
-    std::call_once(attr_once, [] {
-        // the warpgroups' register split (setmaxnreg) adds up to exactly the launch budget: refuse to
-        // launch a build whose per-thread register count differs, rather than let a warpgroup wait
-        // for registers that never come
-        regs_ok = true;
-        for (const void *f : {(const void *)paged_prefill_kernel<false>, (const void *)paged_prefill_kernel<true>}) {
-            if (attr_err == cudaSuccess)
-                attr_err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-            cudaFuncAttributes fa{};
-            if (attr_err == cudaSuccess)
-                attr_err = cudaFuncGetAttributes(&fa, f);
-            regs_ok = regs_ok && attr_err == cudaSuccess && fa.numRegs == kLaunchRegs;
-        }
-    });
-    if (attr_err != cudaSuccess)
+    // Once per device (the shared-memory opt-in is a per-device attribute): set it, and check that
+    // the warpgroups' register split (setmaxnreg) adds up to exactly the launch budget -- a build
+    // whose per-thread register count differs is refused rather than launched, since a warpgroup
+    // would wait for registers that never come.
+    static std::mutex attr_mu;
+    static int attr_state[64];          // 0 not yet, 1 ready, NV_ERR_* the refusal
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return NV_ERR_CUDA;
-    if (!regs_ok)
-        return NV_ERR_UNSUPPORTED;
+    {
+        std::lock_guard<std::mutex> lock(attr_mu);
+        if (attr_state[dev] == 0) {
+            int st = 1;
+            for (const void *f : {(const void *)paged_prefill_kernel<false>, (const void *)paged_prefill_kernel<true>}) {
+                cudaFuncAttributes fa{};
+                if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess ||
+                    cudaFuncGetAttributes(&fa, f) != cudaSuccess) {
+                    st = NV_ERR_CUDA;
+                    break;
+                }
+                if (fa.numRegs != kLaunchRegs)
+                    st = NV_ERR_UNSUPPORTED;
+            }
+            if (st == NV_ERR_CUDA)
+                return st;              // not cached: the next call tries again
+            attr_state[dev] = st;
+        }
+        if (attr_state[dev] != 1)
+            return attr_state[dev];
+    }
     prefill_plan_kernel<<<1, kPlanThreads, 0, a.stream>>>(pp);
     // persistent: one CTA per SM (shared memory and TMEM admit one); CTAs claim the work list's
     // entries in order

@@ -2,6 +2,8 @@
 through its binding, and compare with the oracle under the stated tolerance."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 import workloads as W
@@ -9,6 +11,10 @@ import workloads as W
 # Tolerance for bf16 I/O with fp32 accumulation, against the fp32 oracle.
 MAX_ABS = 2e-2
 MEAN_ABS = 2e-3
+
+# Host threads for the oracle on full-size batches (each thread runs the single-threaded C oracle
+# on its own rows; the arithmetic per row is unchanged).
+ORACLE_THREADS = os.cpu_count() or 8
 
 
 def torch_mod():
@@ -96,6 +102,12 @@ class DeviceBatch:
         torch = torch_mod()
         torch.cuda.synchronize()
         return int(self.d_err.item())
+
+
+def oracle_store_in_place(orc, batch, kc, vc):
+    """The oracle's store applied to host caches in place (for multi-GB pools not needed afterwards)."""
+    orc.store_kvcache(batch.k_new, batch.v_new, batch.slot_mapping, kc, vc)
+    return kc, vc
 
 
 def oracle_cache_after_store(orc, batch, kc, vc):

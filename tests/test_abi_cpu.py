@@ -201,3 +201,41 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         nv.load_library(str(tmp_path / "missing.so"))
+
+
+def test_header_shape_limits(lib):
+    """Every shape limit the header's conventions state, at both sides of each bound.  An accepted
+    shape gets as far as the workspace check (none is passed), which comes before any device work."""
+    # decode: groups 1, 2, 4 (split-KV kernel) and 8, 16 (tile kernel) accepted; 32 and 3 refused
+    for hq, hkv in ((8, 8), (16, 8), (32, 8), (64, 8), (128, 8), (32, 16), (256, 16)):
+        assert _decode(lib, hq=hq, hkv=hkv) == NV_ERR_WORKSPACE, (hq, hkv)
+    for hq, hkv in ((256, 8), (24, 8), (12, 4)):
+        assert _decode(lib, hq=hq, hkv=hkv) == NV_ERR_UNSUPPORTED, (hq, hkv)
+    assert _decode(lib, hq=32, hkv=32) == NV_ERR_UNSUPPORTED      # num_kv_heads above 16
+    assert _decode(lib, hq=20, hkv=8) == NV_ERR_SHAPE             # not a multiple
+    for bs in (16, 32, 64, 128, 256):
+        assert _decode(lib, bs=bs) == NV_ERR_WORKSPACE, bs
+    for bs in (8, 24, 512):
+        assert _decode(lib, bs=bs) == NV_ERR_UNSUPPORTED, bs
+    assert _decode(lib, d=256) == NV_ERR_UNSUPPORTED
+    # decode on the tile kernel (G = 8, 16): num_seqs <= 65535, num_blocks * block_size < 2^31
+    assert _decode(lib, hq=64, hkv=8, B=65535) == NV_ERR_WORKSPACE
+    assert _decode(lib, hq=64, hkv=8, B=65536) == NV_ERR_UNSUPPORTED
+    assert _decode(lib, hq=8, hkv=1, nb=(1 << 23) - 1) == NV_ERR_WORKSPACE
+    assert _decode(lib, hq=8, hkv=1, nb=1 << 23) == NV_ERR_UNSUPPORTED
+    # decode: a pool of fewer than 2^40 values per tensor (2^30 slots of 8 x 128 values)
+    assert _decode(lib, bs=256, nb=(1 << 22) - 1) == NV_ERR_WORKSPACE
+    assert _decode(lib, bs=256, nb=1 << 22) == NV_ERR_UNSUPPORTED
+    # prefill: the same groups, block sizes and head_dim; num_seqs <= 65535
+    for hq, hkv in ((8, 8), (16, 8), (32, 8), (64, 8), (128, 8)):
+        assert _prefill(lib, hq=hq, hkv=hkv, ws=None) == NV_ERR_WORKSPACE, (hq, hkv)
+    assert _prefill(lib, hq=256, hkv=8) == NV_ERR_UNSUPPORTED
+    assert _prefill(lib, hq=24, hkv=8) == NV_ERR_UNSUPPORTED
+    for bs in (16, 256):
+        assert _prefill(lib, bs=bs, ws=None) == NV_ERR_WORKSPACE, bs
+    for bs in (8, 512):
+        assert _prefill(lib, bs=bs) == NV_ERR_UNSUPPORTED, bs
+    assert _prefill(lib, B=65535, ws=None) == NV_ERR_WORKSPACE
+    assert _prefill(lib, B=65536) == NV_ERR_UNSUPPORTED
+    assert _prefill(lib, nb=(1 << 23) - 1, ws=None) == NV_ERR_WORKSPACE
+    assert _prefill(lib, nb=1 << 23) == NV_ERR_UNSUPPORTED

@@ -4,8 +4,8 @@ import pytest
 
 import oracle
 import workloads as W
-from tests.gpu_util import (DeviceBatch, compare, dev_i32, host_bits, host_f32, oracle_cache_after_store,
-                            oracle_decode)
+from tests.gpu_util import (ORACLE_THREADS, DeviceBatch, compare, dev_i32, host_bits, host_f32,
+                            oracle_cache_after_store, oracle_decode, oracle_store_in_place)
 
 pytestmark = pytest.mark.gpu
 
@@ -72,37 +72,34 @@ def test_decode_qwen06_full():
     """256 sequences (L ~ U[100, 2048]) plus 32 graph-padding rows: every real row checked."""
     b = W.qwen06_decode()
     _, got, kc, vc = _run(b)
-    want = oracle_decode(oracle.default(), b, kc, vc, threads=16)
+    want = oracle_decode(oracle.default(), b, kc, vc, threads=ORACLE_THREADS)
     compare(got[:256], want[:256], "qwen06")
     assert not got[256:].any()
 
 
-def _sampled(batch, seqs, label):
+def _full(batch, label):
+    """Store + decode on the GPU, then every real row against the oracle (host threads over rows)."""
     db = DeviceBatch(batch)
     db.store()
     got = host_f32(db.decode())
     assert db.err() == 0
-    sub, ids = batch.subset(seqs)
-    kc, vc = sub.cache(ids)
-    kc, vc = oracle_cache_after_store(oracle.default(), sub, kc, vc)
-    want = oracle_decode(oracle.default(), sub, kc, vc, threads=16)
-    return compare(got[seqs], want, label)
+    kc, vc = oracle_store_in_place(oracle.default(), batch, db.kc_host0, db.vc_host0)
+    want = oracle_decode(oracle.default(), batch, kc, vc, threads=ORACLE_THREADS)
+    real = batch.seq_lens > 0
+    assert not got[~real].any()
+    return compare(got[real], want[real], label)
 
 
-def test_decode_qwen8_full_size_sampled():
-    """The headline batch (512 sequences, L ~ U[1024, 4096], 32/8 heads) at full size; 24 sequences
-    (the longest, the shortest and a random draw) are checked against the oracle."""
-    b = W.qwen8_decode()
-    order = np.argsort(b.seq_lens)
-    rng = np.random.default_rng(0)
-    seqs = sorted(set(order[:4].tolist() + order[-4:].tolist() + rng.choice(512, 16, replace=False).tolist()))
-    _sampled(b, seqs, "qwen8")
+def test_decode_qwen8_full_size():
+    """The headline batch (512 sequences, L ~ U[1024, 4096], 32/8 heads) at full size: every
+    sequence and head compared element by element with the oracle."""
+    _full(W.qwen8_decode(), "qwen8")
 
 
 @pytest.mark.parametrize("bs", [256, 16])
-def test_decode_shared_prefix_sampled(bs):
-    b = W.shared_prefix(block_size=bs)
-    _sampled(b, [0, 1, 31, 63], f"shared-prefix-bs{bs}")
+def test_decode_shared_prefix_full(bs):
+    """64 sequences at context 4096 sharing their first 3072 tokens' blocks: every sequence checked."""
+    _full(W.shared_prefix(block_size=bs), f"shared-prefix-bs{bs}")
 
 
 def test_decode_block_permutation_invariance():

@@ -10,7 +10,8 @@ import pytest
 import oracle
 import paged_kv_attention_store_gb300 as nv
 import workloads as W
-from tests.gpu_util import DeviceBatch, compare, host_bits, host_f32, oracle_cache_after_store, oracle_decode
+from tests.gpu_util import (ORACLE_THREADS, DeviceBatch, compare, host_bits, host_f32, oracle_cache_after_store,
+                            oracle_decode, oracle_store_in_place)
 
 pytestmark = pytest.mark.gpu
 
@@ -72,22 +73,22 @@ def test_fused_qwen06_with_padding_rows():
     fus, got, kc, vc = _fused_vs_separate(b)
     orc = oracle.default()
     kc1, vc1 = oracle_cache_after_store(orc, b, kc, vc)
-    compare(got[:256], oracle_decode(orc, b, kc1, vc1, threads=16)[:256], "qwen06")
+    compare(got[:256], oracle_decode(orc, b, kc1, vc1, threads=ORACLE_THREADS)[:256], "qwen06")
     assert not got[256:].any()
 
 
-def test_fused_qwen8_full_size_sampled():
-    """The headline decode batch at full size, fused; sampled sequences against the oracle."""
+def test_fused_qwen8_full_size():
+    """The headline decode batch at full size through the fused store + decode: the pool equals the
+    oracle's store bit for bit, and every sequence's output matches the oracle."""
     b = W.qwen8_decode()
     fus = DeviceBatch(b)
     got = host_f32(_fused(fus))
     assert fus.err() == 0
-    order = np.argsort(b.seq_lens)
-    seqs = sorted(set(order[:3].tolist() + order[-3:].tolist() + [7, 100, 333]))
-    sub, ids = b.subset(seqs)
     orc = oracle.default()
-    skc, svc = oracle_cache_after_store(orc, sub, *sub.cache(ids))
-    compare(got[seqs], oracle_decode(orc, sub, skc, svc, threads=16), "qwen8 fused")
+    kc, vc = oracle_store_in_place(orc, b, fus.kc_host0, fus.vc_host0)
+    assert np.array_equal(host_bits(fus.k_cache), kc)
+    assert np.array_equal(host_bits(fus.v_cache), vc)
+    compare(got, oracle_decode(orc, b, kc, vc, threads=ORACLE_THREADS), "qwen8 fused")
 
 
 def test_fused_single_key_is_the_new_v_row():

@@ -4,7 +4,8 @@ import pytest
 
 import oracle
 import workloads as W
-from tests.gpu_util import DeviceBatch, compare, host_bits, host_f32, oracle_cache_after_store, oracle_prefill
+from tests.gpu_util import (ORACLE_THREADS, DeviceBatch, compare, host_bits, host_f32, oracle_cache_after_store,
+                            oracle_prefill, oracle_store_in_place)
 
 pytestmark = pytest.mark.gpu
 
@@ -78,23 +79,17 @@ def test_prefill_last_row_equals_decode():
     compare(host_f32(dec), out[last], "decode vs last prefill row")
 
 
-def test_prefill_chunk_budget_full_size_sampled():
+def test_prefill_chunk_budget_full_size():
     """The chunked-prefill workload at full size (16 sequences, 16384 new tokens, prefixes up to
-    2048): rows sampled at the start, end and tile edges of every sequence plus a random draw."""
+    2048): every query row and head compared element by element with the oracle."""
     b = W.prefill_chunk()
-    db, got, kc, vc = _run(b)
-    cu = b.cu_seqlens_q
-    rows = set()
-    rng = np.random.default_rng(1)
-    for s in range(b.num_seqs):
-        lo, hi = int(cu[s]), int(cu[s + 1])
-        for r in (lo, lo + 1, lo + 63, lo + 64, hi - 65, hi - 2, hi - 1):
-            if lo <= r < hi:
-                rows.add(r)
-    rows |= set(rng.choice(int(cu[-1]), 96, replace=False).tolist())
-    rows = np.array(sorted(rows), np.int64)
-    want = oracle_prefill(oracle.default(), b, kc, vc, rows=rows, threads=16)
-    compare(got[rows], want, "prefill chunk budget")
+    db = DeviceBatch(b)
+    db.store()
+    got = host_f32(db.prefill())
+    assert db.err() == 0
+    kc, vc = oracle_store_in_place(oracle.default(), b, db.kc_host0, db.vc_host0)
+    want = oracle_prefill(oracle.default(), b, kc, vc, threads=ORACLE_THREADS)
+    compare(got, want, "prefill chunk budget")
 
 
 def test_prefill_grid_hint_smaller_than_chunk_is_flagged():
@@ -122,5 +117,5 @@ def test_prefill_many_sequences_and_long_chunk_sampled():
     rows |= {lo, lo + 63, lo + 64, lo + 2047, lo + 2048, lo + 2111, lo + 2112, lo + 2499}
     rows |= set((lo + rng.choice(2500, 40, replace=False)).tolist())
     rows = np.array(sorted(rows), np.int64)
-    want = oracle_prefill(oracle.default(), b, kc, vc, rows=rows, threads=16)
+    want = oracle_prefill(oracle.default(), b, kc, vc, rows=rows, threads=ORACLE_THREADS)
     compare(got[rows], want, "prefill many sequences")

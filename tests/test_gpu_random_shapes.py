@@ -6,7 +6,8 @@ import pytest
 
 import oracle
 import workloads as W
-from tests.gpu_util import DeviceBatch, compare, host_f32, oracle_cache_after_store, oracle_decode, oracle_prefill
+from tests.gpu_util import (ORACLE_THREADS, DeviceBatch, compare, host_f32, oracle_cache_after_store, oracle_decode,
+                            oracle_prefill)
 
 pytestmark = pytest.mark.gpu
 
@@ -58,4 +59,4 @@ def test_prefill_random_shapes(seed):
     got = host_f32(db.prefill())
     assert db.err() == 0
     kc, vc = oracle_cache_after_store(oracle.default(), b, db.kc_host0, db.vc_host0)
-    compare(got, oracle_prefill(oracle.default(), b, kc, vc, threads=16), b.name)
+    compare(got, oracle_prefill(oracle.default(), b, kc, vc, threads=ORACLE_THREADS), b.name)

@@ -68,6 +68,50 @@ def test_noalloc_matches_allocating_entry_point_twice(make):
         assert not got[~rows].any()
 
 
+def test_noalloc_headline_batch_coarsened_split_against_oracle():
+    """The 512-sequence headline batch: its usual split (512 positions, 8 per sequence) needs more
+    partials than the static array holds, so the entry point doubles the split until they fit.  Every
+    sequence of that coarsened-split result is compared with the oracle itself."""
+    import torch
+    import oracle
+    from tests.gpu_util import ORACLE_THREADS, oracle_decode, oracle_store_in_place
+    b = W.qwen8_decode()
+    db = DeviceBatch(b)
+    db.store()
+    max_ctx = int(b.seq_lens.max())
+    out = torch.full_like(db.q, float("nan"))
+    assert _call(_c_entry(), db, out, max_ctx) == 0
+    got = host_f32(out)
+    assert db.err() == 0
+    kc, vc = oracle_store_in_place(oracle.default(), b, db.kc_host0, db.vc_host0)
+    compare(got, oracle_decode(oracle.default(), b, kc, vc, threads=ORACLE_THREADS), "noalloc qwen8 vs oracle")
+
+
+def test_noalloc_many_splits_use_the_merge_launch():
+    """Three long contexts in a tiny batch are cut into 64-position splits (up to 128 per sequence),
+    more than the decode kernel merges itself, so the partials in the static array are combined by
+    the separate merge launch.  Two calls in a row against the allocating entry point and the oracle."""
+    import torch
+    import oracle
+    from tests.gpu_util import oracle_cache_after_store, oracle_decode
+    b = W.make_decode("long3", 5, [8192, 7999, 5000], 32, 8, 128, 256)
+    db = DeviceBatch(b)
+    db.store()
+    max_ctx = int(b.seq_lens.max())
+    want = host_f32(db.decode(max_context_len=max_ctx))
+    assert db.err() == 0
+    kc, vc = oracle_cache_after_store(oracle.default(), b, db.kc_host0, db.vc_host0)
+    ref = oracle_decode(oracle.default(), b, kc, vc)
+    f = _c_entry()
+    for call in range(2):
+        out = torch.full_like(db.q, float("nan"))
+        assert _call(f, db, out, max_ctx) == 0
+        got = host_f32(out)
+        assert db.err() == 0
+        compare(got, want, f"noalloc many splits, call {call}")
+        compare(got, ref, f"noalloc many splits vs oracle, call {call}")
+
+
 def test_noalloc_rejects_a_batch_beyond_the_static_array():
     """1024 sequences x 64 q heads (16 kv heads: group 4, the split-KV kernel) x 8192 positions need
     more partials than the array holds even at the longest split: rejected on the host, nothing
