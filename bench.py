@@ -505,6 +505,7 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         extra_steps = max(5, min(args.steps, 50))
         cfg_q06 = measure_decode_config(W.qwen06_decode(seed=rank), extra_steps, args.warmup, dev)
+        cfg_64 = measure_decode_config(W.qwen8_decode(seed=rank, num_seqs=64), extra_steps, args.warmup, dev)
         cfg_sp = {bs: measure_decode_config(W.shared_prefix(seed=rank, block_size=bs), extra_steps, args.warmup, dev)
                   for bs in (256, 16)}
     finally:
@@ -623,8 +624,10 @@ def run_ours(args, rank, world, local_rank):
                              "per step); all timed phases together: see gpu_launches_all_phases",
         # per step: headline and e2e (store + decode each), fused (1), prepare_decode (1), sampler (1), prefill
         # (store + pre-pass + attention), prologue (1); then the decode call of the three extra configs
+        # (the extra configs: qwen06 one split-KV launch; the 64-sequence and shared-prefix batches a
+        # pre-pass and the tile kernel each)
         "gpu_launches_all_phases": (launches_per_decode_step * 2 + 1 + 1 + 1 + 3 + 1) * args.steps
-                                   + 3 * max(5, min(args.steps, 50)),
+                                   + (1 + 2 + 2 + 2) * max(5, min(args.steps, 50)),
         "clocks": clocks,
         "prefill": {
             "workload": "chunked prefill with prefix cache (store 16384 new rows + causal varlen prefill): 16 seqs, "
@@ -648,9 +651,15 @@ def run_ours(args, rank, world, local_rank):
                         "graph-padding rows (slot -1, context 0); store 288 rows + decode",
             **cfg_q06, "hbm_frac_of_peak": round(cfg_q06["logical_kv_gbs"] / hbm_peak, 4),
         },
+        "qwen8_decode_64seq": {
+            "workload": "the Qwen3-8B decode shape with 64 sequences (ctx U[1024, 4096], 32 q / 8 kv heads, bs 256); "
+                        "store 64 rows + decode, which runs on the tcgen05 tile kernel (a split-KV grid this short "
+                        "ends in a partly filled wave)",
+            **cfg_64, "hbm_frac_of_peak": round(cfg_64["logical_kv_gbs"] / hbm_peak, 4),
+        },
         "shared_prefix": {
             "workload": "64 seqs at context 4096, 32 q / 8 kv heads, the first 3072 tokens in the same physical "
-                        "blocks; logical KV 1.07 GB, unique 281 MB",
+                        "blocks; logical KV 1.07 GB, unique 281 MB; decode on the tcgen05 tile kernel",
             "bs256": cfg_sp[256], "bs16": cfg_sp[16],
             "bs16_slowdown": round(cfg_sp[16]["ms_per_decode"] / cfg_sp[256]["ms_per_decode"], 3),
         },
@@ -808,11 +817,12 @@ def run_reference(args, rank, world):
 def run_profile_case(case: str):
     """Run one small case three times (store + attention) for an ncu capture, then exit.
 
-    decode-64seq: the first 64 sequences' shapes of the Qwen3-8B decode batch (about 0.7 GB of
-    KV, above the 129 MB L2, a few GB on the device in all); decode-g8-64seq: the same lengths with
-    64 query heads over the 8 kv heads (Qwen3-32B's attention shape, group 8); decode-512seq: the headline batch
-    itself (for one-pass DRAM counters only); prefill-chunk: the full chunked-prefill workload
-    (about 0.3 GB)."""
+    decode-16seq: the first 16 sequences' shapes of the Qwen3-8B decode batch (about 170 MB of KV,
+    above the 129 MB L2), which decode on the same split-KV kernel as the full 512-sequence batch;
+    decode-64seq: the first 64 sequences (about 0.7 GB of KV), which decode on the tile kernel;
+    decode-g8-64seq: the same lengths with 64 query heads over the 8 kv heads (Qwen3-32B's attention
+    shape, group 8); prefill-chunk: the full chunked-prefill workload (about 0.3 GB).  Each holds
+    a few GB on the device at most."""
     import torch
 
     import paged_kv_attention_store_gb300 as nv
@@ -837,14 +847,13 @@ def run_profile_case(case: str):
         print(json.dumps({"profile_case": case, "d_err": int(d_err.item()),
                           "algorithmic_bytes": 256 * 151936 * 6 + 256 * 12}))
         return
-    if case == "decode-64seq":
-        ctx = np.random.default_rng([0, 200]).integers(1024, 4097, size=512)[:64]
-        b = W.make_decode("qwen3-8b-decode-64", 0, ctx, 32, 8, 128, 256)
+    if case in ("decode-16seq", "decode-64seq"):
+        n = 16 if case == "decode-16seq" else 64
+        ctx = np.random.default_rng([0, 200]).integers(1024, 4097, size=512)[:n]
+        b = W.make_decode(f"qwen3-8b-decode-{n}", 0, ctx, 32, 8, 128, 256)
     elif case == "decode-g8-64seq":
         ctx = np.random.default_rng([0, 200]).integers(1024, 4097, size=512)[:64]
         b = W.make_decode("group8-decode-64", 0, ctx, 64, 8, 128, 256)
-    elif case == "decode-512seq":
-        b = W.qwen8_decode(seed=0)     # the headline batch (about 13 GB on the device)
     elif case.startswith("shared-prefix-bs"):
         b = W.shared_prefix(block_size=int(case[len("shared-prefix-bs"):]))
     else:
@@ -890,7 +899,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work per oracle baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seqs-per-step", type=int, default=1)
-    ap.add_argument("--profile-case", choices=["decode-64seq", "decode-g8-64seq", "decode-512seq", "prefill-chunk", "prologue-chunk",
+    ap.add_argument("--profile-case", choices=["decode-16seq", "decode-64seq", "decode-g8-64seq", "prefill-chunk", "prologue-chunk",
                                                "sampler-256rows",
                                                "shared-prefix-bs256", "shared-prefix-bs16"],
                     help="run one small case three times for an ncu capture and exit")

@@ -211,14 +211,19 @@ size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
  * block_size + j % block_size.  fp32 accumulation and softmax, bf16 output rounded once.
  * A row with L == 0 (graph padding) gets zeros.
  *
- * Groups (num_q_heads / num_kv_heads) 1, 2, 4: a split-KV flash-decoding kernel on CUDA cores (one
- * launch; a second one merges the partials when a sequence spans more than 16 splits).  Groups 8 and 16: each query head of a group multiplies every KV byte, and the CUDA-core
- * kernel's FMAs no longer keep up with HBM (measured 0.54 of the roofline at group 8), so the call
- * runs the tcgen05 tile kernel of nv_paged_prefill_attn with one query row per sequence at position
- * L-1 (two launches: a work-list pre-pass, which also zeroes the rows with L == 0, and the tile
- * kernel; a batch with fewer than two (sequence, kv head) units per SM has its keys split into
- * ranges of at least 1024, and a third launch merges them).  The two paths round differently (both
- * within the parity bar of the fp32 definition).
+ * Groups (num_q_heads / num_kv_heads) 1 and 2, and group 4 for batches of at most 16 sequences or
+ * whose split-KV grid spans at least ten waves of the GPU (the 512-sequence Qwen3-8B batch): a
+ * split-KV flash-decoding kernel on CUDA cores (one launch; a second one merges the partials when a
+ * sequence spans more than 16 splits).  Groups 8 and 16, and group 4 in between: the tcgen05 tile
+ * kernel of nv_paged_prefill_attn with one query row per sequence at position L-1 (two launches: a
+ * work-list pre-pass, which also zeroes the rows with L == 0, and the tile kernel; a batch with
+ * fewer than two (sequence, kv head) units per SM has its keys split into ranges of at least 1024,
+ * and a third launch merges them).  At group 8 the CUDA-core kernel's FMAs no longer keep up with
+ * HBM (measured 0.54 of the roofline); at group 4 the tile kernel's persistent schedule fills the
+ * GPU where a short split-KV grid cannot (64 sequences: 109 against 150 us), and it keeps up when
+ * shared prefix blocks come from L2 and the CUDA-core consumers are bound by their FMAs.  The two
+ * paths round differently (P is rounded to bf16 before the PV product on the tile kernel); both
+ * are within the parity bar of the fp32 definition.
  *
  *   q, out        bf16 [num_seqs, num_q_heads, head_dim], contiguous, 16-byte aligned.
  *   block_tables  int32 [num_seqs, bt_stride]; context_lens int32 [num_seqs].

@@ -675,6 +675,30 @@ int run_split_kv(int group, DecodeParams &p, int num_seqs, cudaStream_t st)
 // about 1.0 for the tile kernel on the same batch).  Its work list sits after the split counters.
 constexpr int kTileGroup = 8;
 
+// Which kernel decodes a batch.  G >= 8: the tile kernel (above).  G = 4: the split-KV kernel for
+// batches whose grid spans at least ten waves of the GPU (two CTAs per SM), and for batches of at
+// most 16 sequences; the tile kernel in between.  Measured at G = 4 (32 q / 8 kv heads, contexts
+// U[1024, 4096]): the split-KV grid of a mid-sized batch ends in a partly filled last wave and
+// pays each CTA's start (barriers, a pipeline refilled from HBM) per (sequence, split): 64
+// sequences 149.5 us (4.3 TB/s) against 109.2 us (5.9 TB/s) on the tile kernel, whose persistent
+// CTAs claim (sequence, kv head) units and split long keys into ranges; 256 sequences 437 against
+// 392 us; and when most of the KV is shared and sits in L2 (64 sequences sharing 3072 of their
+// 4096 positions) the split-KV consumers are bound by their own FMAs: 172 against 123 us.  The
+// headline-sized batch (512 sequences, 13 waves) is HBM-bound on CUDA cores at 0.98 of the copy
+// peak and stays there; at 16 sequences or fewer the split-KV kernel is the faster one (51 against
+// 56 us at 8).  G = 1, 2 always use the split-KV kernel (G = 2, 256 sequences: 180 against 189 us).
+bool decode_on_tiles_rule(int group, int num_seqs, int max_context_len)
+{
+    if (group >= kTileGroup)
+        return true;
+    if (group != 4 || num_seqs <= 16)
+        return false;
+    const int split = decode_split_tokens(num_seqs, max_context_len);
+    const int64_t units = (int64_t)num_seqs * ((max_context_len + split - 1) / split);
+    const int sms = nvkv_host::sm_count();
+    return sms > 0 && units < 10 * 2 * (int64_t)sms;
+}
+
 // The tile kernel's own limits (its work list packs sequence ids and pool slots in 16 and 31 bits),
 // checked before the workspace so the refusal does not depend on it.
 bool tile_shape_ok(int32_t num_seqs, int32_t num_blocks, int32_t block_size)
@@ -869,7 +893,7 @@ int decode_entry(const void *q, const void *k_cache, const void *v_cache, const 
         p.v_cache_w = static_cast<__nv_bfloat16 *>(const_cast<void *>(v_cache));
         p.num_slots = (int64_t)num_blocks * block_size;
     }
-    if (group >= kTileGroup) {
+    if (decode_on_tiles_rule(group, num_seqs, max_context_len)) {
         if (!tile_shape_ok(num_seqs, num_blocks, block_size))
             return NV_ERR_UNSUPPORTED;
         if (!workspace || workspace_bytes < kCounterBytes + tile_list_bytes(num_seqs) || !aligned16(workspace))
@@ -999,7 +1023,7 @@ extern "C" int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, 
         max_context_len = 1;
     const int64_t bt_cap = (int64_t)bt_stride * block_size;
     const int max_len = (int)(bt_cap < max_context_len ? bt_cap : max_context_len);
-    if (group >= kTileGroup) {     // the tile kernel's work list goes in the static array
+    if (decode_on_tiles_rule(group, num_seqs, max_context_len)) {   // the work list goes in the static array
         if (!tile_shape_ok(num_seqs, num_blocks, block_size))
             return NV_ERR_UNSUPPORTED;
         void *scratch = nullptr;

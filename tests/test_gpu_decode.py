@@ -102,6 +102,13 @@ def test_decode_shared_prefix_full(bs):
     _full(W.shared_prefix(block_size=bs), f"shared-prefix-bs{bs}")
 
 
+@pytest.mark.parametrize("num_seqs", [17, 64, 200])
+def test_decode_group4_mid_batches_on_tiles(num_seqs):
+    """Group 4 batches of 17 to a few hundred sequences decode on the tcgen05 tile kernel (their
+    split-KV grid would end in a partly filled wave): every sequence against the oracle."""
+    _full(W.qwen8_decode(num_seqs=num_seqs), f"group4 {num_seqs} seqs")
+
+
 def test_decode_block_permutation_invariance():
     b = W.make_decode("perm", 23, [40, 700, 1200], 16, 8, 128, 64)
     db, got, kc, vc = _run(b)
@@ -181,14 +188,15 @@ def test_decode_workspace_reused_across_batches_and_after_an_error():
 
 def test_decode_workspace_not_zero_filled_is_flagged():
     """Split counters that do not start at zero (a workspace that was not zero-filled) are reported.
-    100 sequences of 1024 positions split 8 ways, so the last split of each merges in the kernel
-    through the counters (above 16 splits a merge launch combines them, and no counter is used)."""
+    100 sequences of 1024 positions at group 2 (always the split-KV kernel) split 8 ways, so the last
+    split of each merges in the kernel through the counters (above 16 splits a merge launch combines
+    them, and no counter is used)."""
     import torch
     import paged_kv_attention_store_gb300 as nv
-    b = W.make_decode("dirty-ws", 29, [1024] * 100, 8, 2, 128, 64)
+    b = W.make_decode("dirty-ws", 29, [1024] * 100, 4, 2, 128, 64)
     db = DeviceBatch(b)
     db.store()
-    ws = torch.full((nv.nv_paged_decode_workspace_size(b.num_seqs, 8, 128, 1024),), 0xFF, dtype=torch.uint8,
+    ws = torch.full((nv.nv_paged_decode_workspace_size(b.num_seqs, 4, 128, 1024),), 0xFF, dtype=torch.uint8,
                     device="cuda")
     nv.nv_paged_decode_attn(db.q, db.k_cache, db.v_cache, db.block_tables, db.seq_lens, b.scale,
                             max_context_len=1024, workspace=ws, d_err=db.d_err)

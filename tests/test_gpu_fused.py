@@ -51,6 +51,9 @@ CASES = [
     ("g8-hkv8", [1, 257, 1100, 3000], 64, 8, 256, 1),   # store pass + tile kernel, keys split
     ("g8-long", [5, 9000], 64, 8, 64, 0),
     ("g4-hkv12", [4, 129, 700], 48, 12, 32, 0),
+    # group 4 with 17-40 sequences decodes on the tile kernel: store pass + tile decode
+    ("g4-tiles-24", list(np.random.default_rng(5).integers(1, 3000, 24)), 32, 8, 128, 2),
+    ("g4-tiles-40-bs16", list(np.random.default_rng(6).integers(1, 2000, 40)), 32, 8, 16, 0),
 ]
 
 

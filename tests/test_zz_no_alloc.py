@@ -47,8 +47,12 @@ def _group16():
     return W.make_decode("group16", 4, [1, 300, 2048, 700], 128, 8, 128, 16, n_pad=2)
 
 
-@pytest.mark.parametrize("make", [W.qwen06_decode, W.qwen8_decode, _group8, _group16],
-                         ids=["qwen3-0.6b", "qwen3-8b", "group8-tiles", "group16-tiles"])
+def _group4_mid():
+    return W.qwen8_decode(num_seqs=64)
+
+
+@pytest.mark.parametrize("make", [W.qwen06_decode, W.qwen8_decode, _group8, _group16, _group4_mid],
+                         ids=["qwen3-0.6b", "qwen3-8b", "group8-tiles", "group16-tiles", "group4-64seq-tiles"])
 def test_noalloc_matches_allocating_entry_point_twice(make):
     import torch
     b = make()
