@@ -117,27 +117,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Non-blocking test of up to three phases at once (pass a barrier twice to test fewer): the three
-// reads of the barriers are in flight together, so a check of already-completed phases costs one
-// shared-memory round trip instead of three.
-__device__ __forceinline__ bool mbar_test3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, uint32_t b2,
-                                           uint32_t p2)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred q0, q1, q2;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
-        "and.pred q0, q0, q1;\n\t"
-        "and.pred q0, q0, q2;\n\t"
-        "selp.u32 %0, 1, 0, q0;\n\t}"
-        : "=r"(ok)
-        : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
-        : "memory");
-    return ok != 0;
-}
-
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
     uint64_t t;

@@ -95,7 +95,8 @@ constexpr int kNumBars = kBarDrain + 2;
 constexpr uint32_t kOffItems = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffRowSum = kOffItems + kQueue * kItemInts * 4;   // float [2 item parities][128 rows]
 constexpr uint32_t kOffTmemSlot = kOffRowSum + 2 * 128 * 4;
-constexpr uint32_t kSmemBytes = kOffTmemSlot + 16 + 1024;      // + slack for 1024-byte alignment
+// TMEM address, abort flag, then the copies the producers attempted (K, Q, V), for the drain
+constexpr uint32_t kSmemBytes = kOffTmemSlot + 32 + 1024;      // + slack for 1024-byte alignment
 static_assert(kSmemBytes <= 227u * 1024u, "shared memory per CTA");
 
 struct PrefillParams {
@@ -391,13 +392,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar = base + kOffBar;
     auto BAR = [&](int i) { return bar + 8u * (uint32_t)i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffTmemSlot);
-    // set by any warp whose bounded wait gave up: the CTA then lets its copies and MMAs land before it
-    // frees tensor memory and leaves
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffTmemSlot + 4);
-    // copies this CTA's producers issued (warp-uniform in the producer warps), for that drain
-    int k_copies = 0, q_copies = 0, v_copies = 0;
+    // Shared words after the TMEM address: [1] set by any warp whose bounded wait gave up (the CTA
+    // then lets its copies and MMAs land before it frees tensor memory and leaves); [2..4] the copies
+    // the producers attempted (K, Q, V), for that drain.  Addressed from `base`, so that no other
+    // register stays live in every warp for them.
+    auto word = [&](int i) { return base + kOffTmemSlot + 4u * (uint32_t)i; };
+    auto st_word = [](uint32_t a, int v) { asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory"); };
+    auto ld_word = [](uint32_t a) {
+        int v;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+        return v;
+    };
     auto give_up = [&]() {
-        *abort_flag = 1;
+        st_word(word(1), 1);
         flag_error(p.d_err, NV_DERR_TIMEOUT);
     };
 
@@ -425,7 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(BAR(kBarDrain), 1);
         mbar_init(BAR(kBarDrain + 1), 1);
-        *abort_flag = 0;
+        for (int i = 1; i <= 4; ++i)
+            st_word(word(i), 0);
         fence_barrier_init();
     }
     // Work items pass from the producer (which claims them) to the MMA issuer's two cursors and
@@ -625,7 +633,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(dst, map, 0, kvh, slot, full);
                 tma_load_3d(dst + kHalf, map, 64, kvh, slot, full);
             }
-            ++(is_v ? v_copies : k_copies);
             return true;
         };
         if (warp == kWarpProducer) {
@@ -717,11 +724,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 tma_load_3d(base + kOffQ + qb * kTile + h * kHalf, &tmap_q, h * 64,
                                             it.kvh * p.group, it.cq0 + it.i0, BAR(kBarQFull + qb));
                         }
-                        ++q_copies;
+                        if (lane == 0)
+                            st_word(word(3), k + 1);
                     }
                     ok = copy_tile(false, j, it.kvh, slot);
                 }
             }
+            if (lane == 0)
+                st_word(word(2), j);    // K copies attempted (after a wait gave up: one more than issued)
             if (!ok && lane == 0)
                 give_up();
         } else if (warp == kWarpVProducer) {
@@ -747,6 +757,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int n = 0; n < it.nkv && ok; ++n, ++j)
                     ok = copy_tile(true, j, it.kvh, box_slot(it, n, bt, nblk, win_base, win));
             }
+            if (lane == 0)
+                st_word(word(4), j);    // as for K
             if (!ok && lane == 0)
                 give_up();
         } else if (warp == kWarpS || warp == kWarpPV) {
@@ -754,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Key steps of all this CTA's work items form one global sequence g.  S(g) goes to TMEM
             // buffer g % 3 once PV(g-3) has finished with it; both streams run across tile
             // boundaries, so the next tile's first scores are computed during the current tile's last
-            // softmax.  (Single-issuer build: the order S(0) S(1) | PV(g) S(g+2) | ...)
+            // softmax.
             constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);   // Q, K both K-major
             constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, kD, false, true);     // P (TMEM), V MN-major
             // Operand descriptors of Q buffer 0 and K / V slot 0; the others differ only in the start
@@ -986,21 +998,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // On the normal path every copy and MMA this CTA issued has been waited for by the warp that
     // consumes it.  After a wait gave up that no longer holds: copies may still be landing in shared
     // memory and MMAs still reading it and writing tensor memory.  So each producer waits for the
-    // copies it issued last (one per ring slot: all earlier ones were consumed, or their slot reused
-    // after they landed), each issuing thread commits its MMAs to a barrier of its own and waits
-    // for it, and only then is tensor memory freed and the CTA's shared memory released.  Every
-    // wait is bounded as usual.
+    // copies it attempted last (one per ring slot: all earlier ones were consumed, or their slot
+    // reused after they landed; a copy whose slot wait gave up was never issued, and its wait here
+    // just runs out), each issuing thread commits its MMAs to a barrier of its own and waits for it,
+    // and only then is tensor memory freed and the CTA's shared memory released.  Every wait is
+    // bounded as usual.
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag) {
+    if (ld_word(word(1))) {
         if (lane == 0) {
             if (warp == kWarpProducer) {
-                for (int i = max(0, k_copies - kKSlots); i < k_copies; ++i)
+                const int nk = ld_word(word(2)), nq = ld_word(word(3));
+                for (int i = max(0, nk - kKSlots); i < nk; ++i)
                     mbar_wait(BAR(kBarKFull + i % kKSlots), (i / kKSlots) & 1);
-                for (int i = max(0, q_copies - kQBufs); i < q_copies; ++i)
+                for (int i = max(0, nq - kQBufs); i < nq; ++i)
                     mbar_wait(BAR(kBarQFull + i % kQBufs), (i / kQBufs) & 1);
             } else if (warp == kWarpVProducer) {
-                for (int i = max(0, v_copies - kVSlots); i < v_copies; ++i)
+                const int nv = ld_word(word(4));
+                for (int i = max(0, nv - kVSlots); i < nv; ++i)
                     mbar_wait(BAR(kBarVFull + i % kVSlots), (i / kVSlots) & 1);
             } else if (warp == kWarpS || warp == kWarpPV) {
                 mma_commit(BAR(kBarDrain + (warp - kWarpS)));
