@@ -398,9 +398,8 @@ def nv_store_decode_attn(q, k, v, slot_mapping, k_cache, v_cache, block_tables, 
     attention over the history that ends with it, in one pass (same result as ``nv_store_kvcache``
     then ``nv_paged_decode_attn``).  ``workspace`` as for ``nv_paged_decode_attn``."""
     nb, bs, hkv, d = _pool_shape(k_cache, v_cache)
-    B, hq, dq = (int(x) for x in q.shape)
-    _need(dq == d and q.is_contiguous(), "q must be contiguous [B, Hq, D]")
-    _table(block_tables, B)
+    _need(q.dim() == 3, "q must be contiguous [B, Hq, D]")
+    B = int(q.shape[0])
     _need(slot_mapping.dim() == 1 and int(slot_mapping.shape[0]) == B,
           "slot_mapping must have one entry per sequence")
     _vec(slot_mapping, "slot_mapping", B)
