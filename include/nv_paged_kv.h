@@ -64,7 +64,7 @@ typedef enum nv_status {
 #define NV_DERR_SLOT_RANGE 0x1    /* slot_mapping entry < -1 or >= num_slots: row skipped */
 #define NV_DERR_BLOCK_RANGE 0x2   /* a needed block-table entry outside [0, num_blocks): nothing is read
                                      from it; that sequence's output is not meaningful (the store and
-                                     the split-KV decode of groups 1-4 skip its keys) */
+                                     the split-KV decode kernel skip its keys) */
 #define NV_DERR_LENGTH 0x4        /* a length exceeds the block table, the host hint, or is negative */
 #define NV_DERR_TIMEOUT 0x8       /* a bounded wait on an asynchronous copy gave up */
 #define NV_DERR_SLOT_MISMATCH 0x10 /* fused store + decode: a slot that is not position L-1's (row not stored) */
@@ -193,8 +193,8 @@ int nv_sample_exponential_race(const void *logits, int64_t logits_stride, const 
 
 /*
  * Bytes of workspace nv_paged_decode_attn needs for this batch: 256 KiB of split counters, then the
- * larger of the split-KV partials (groups 1-4; none when one split covers max_context_len) and the
- * tile kernel's work list (groups 8 and 16: 64 bytes + 32 per sequence).  Depends only on its
+ * larger of the split-KV partials (none when one split covers max_context_len) and the tile kernel's
+ * partials and work list (64 bytes + 32 per sequence and split).  Depends only on its
  * arguments, so it can be sized once for the largest batch and reused.
  */
 size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t head_dim,
@@ -233,7 +233,8 @@ size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
  *                 truncated to it and flagged NV_DERR_LENGTH.  <= bt_stride*block_size.
  *   scale         softmax scale (head_dim ** -0.5 in the pages).
  *   workspace     device scratch of at least nv_paged_decode_workspace_size(...) bytes, 16-byte
- *                 aligned (groups 1-4 may pass NULL when one split covers max_context_len).  Its first 256 KiB hold
+ *                 aligned (a batch on the split-KV kernel may pass NULL when one split covers
+ *                 max_context_len; the tile kernel always needs one for its work list).  Its first 256 KiB hold
  *                 the per-sequence split counters: they must be ZERO before the first call
  *                 that uses the workspace (allocate it zero-filled), and every call leaves them
  *                 zero, whatever the batch; the rest needs no initialisation.  A counter found
