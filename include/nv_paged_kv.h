@@ -293,12 +293,12 @@ int nv_store_decode_attn(const void *q, const void *k, int64_t k_row_stride, con
  * partials live in a fixed device array of NV_DECODE_STATIC_SCRATCH_BYTES inside the library,
  * which every GPU that loads the library holds until the process exits.
  *
- * Arguments and results are those of nv_paged_decode_attn (same kernels; groups 8 and 16 keep the
- * tile kernel's work list, and its split partials when a batch's keys are split, in the same static
- * array, and do not split when they would not fit).  The split length
- * is the usual one, doubled (up to 4096 positions) while the partials would not fit the
- * array; a batch whose partials still exceed it (num_seqs * splits * num_q_heads * 520 bytes)
- * is rejected with NV_ERR_WORKSPACE before anything is enqueued.
+ * Arguments and results are those of nv_paged_decode_attn (same kernels, chosen the same way; a
+ * batch that decodes on the tile kernel keeps its work list, and its split partials when its keys are
+ * split, in the same static array, and does not split when they would not fit).  On the split-KV
+ * kernel the split length is the usual one, doubled (up to 4096 positions) while the partials would
+ * not fit the array; a batch whose partials still exceed it (num_seqs * splits * num_q_heads * 520
+ * bytes) is rejected with NV_ERR_WORKSPACE before anything is enqueued.
  *
  * The first call on a device looks up the arrays' device addresses (cudaGetSymbolAddress) with
  * that device current; make that first call before any stream capture.  All calls share the
