@@ -13,7 +13,8 @@
 // the next tile's first scores are computed while the current tile finishes.
 //   * a one-CTA pre-pass lists the non-empty query tiles in the caller's workspace, sequence by
 //     sequence (heaviest sequence first, each sequence's tiles heaviest first), so the CTAs at
-//     work share a few sequences' K/V in L2; a claim is one atomic add on a counter there.
+//     work share a few sequences' K/V in L2; CTA i takes claim i first, and every later claim
+//     is one atomic add on a counter there.
 //   * warps 4 and 11 (TMA producers): warp 4 claims tiles and passes them to the other warps
 //     through a small queue in shared memory, and copies each tile's Q (one 3-D tensor-map copy
 //     per 64-dim half; dims head_dim, q head, token) into one of two Q buffers and its K tiles
@@ -197,14 +198,16 @@ struct Item {
 
 // ---------------------------------------------------------------------------------------
 // Work list.  A one-CTA pre-pass lists every non-empty query tile of every sequence (all kv
-// heads share an entry) in the workspace, validates the lengths, and zeroes the claim counter.
+// heads share an entry) in the workspace, validates the lengths, and starts the claim counter at
+// the main kernel's grid size: CTA i's first claim is i itself, so the first items of all CTAs are
+// not serialised on one atomic as the CTAs start together.
 // The list runs sequence by sequence, heaviest sequence first (a counting sort on the key steps
 // of its last tile), and within a sequence from its last (heaviest) tile to its first.  So the
 // CTAs busy at any moment work on one or two sequences, whose K/V then stays in L2 while every
 // tile of the sequence reads it (ordering all tiles by weight alone instead streamed the whole
 // batch's K/V from HBM once per wave), and the lightest tiles still come last.  The main
-// kernel's claim number v then names entry v / Hkv and kv head v % Hkv: a claim is one atomic
-// add and one 32-byte record load, with no empty tiles to skip.
+// kernel's claim number v then names entry v / Hkv and kv head v % Hkv: a claim is at most one
+// atomic add and one 32-byte record load, with no empty tiles to skip.
 //   workspace ints: [0] claim counter, [1] entries, [16 + 8e ...] entry e:
 //   {b, cq0, Lq, P, i0, nq, kv_len, nkv}
 // ---------------------------------------------------------------------------------------
@@ -223,6 +226,7 @@ struct PlanParams {
     int32_t max_len;         // decode mode: longer contexts are truncated to this (NV_DERR_LENGTH)
     int32_t row_u4;          // decode mode: 16-byte words per output row
     int32_t split_steps;     // decode mode: key steps per entry (0: one entry per sequence)
+    int32_t grid;            // CTAs of the main kernel: claims below it are taken by CTA index
 };
 
 __device__ __forceinline__ bool plan_seq(const PlanParams &pp, int b, int &cq0, int &Lq, int &P, int &T)
@@ -367,7 +371,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const Pla
     if (tid == 0) {
         if (count > pp.cap)
             flag_error(pp.d_err, NV_DERR_LENGTH);
-        pp.ws[0] = 0;
+        pp.ws[0] = pp.grid;
         pp.ws[1] = min(count, pp.cap);
     }
 }
@@ -476,6 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     // The work list comes from the pre-pass launched just before; this kernel is its programmatic
     // dependent, so the setup above overlapped it.
+    if (warp == kWarpProducer && lane == 0) {    // kernel parameters: fetch them during the pre-pass
+        prefetch_tmap(&tmap_q);
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+        prefetch_tmap(&tmap_o);
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     total = p.ws[1] * p.num_kv_heads;
     if (warp < 4) {
@@ -640,19 +650,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Claims items and queues them; copies each item's Q tile (one 3-D tensor-map copy
             // per 64-dim half) into one of two Q buffers just before the item's first K tile, and
             // its K tiles into the K ring as the S issuer frees the slots.
-            if (lane == 0) {
-                prefetch_tmap(&tmap_q);
-                prefetch_tmap(&tmap_k);
-                prefetch_tmap(&tmap_o);
-            }
             bool ok = true;
             int j = 0;                                  // global key tile of the next K copy
             // lane 0 claims one item ahead: the counter's answer for item k+1 travels while item k's
-            // copies are issued
+            // copies are issued.  The first claim is the CTA's index (the counter starts at the grid
+            // size).
             const int4 *plan = reinterpret_cast<const int4 *>(p.ws + kPlanHeaderInts);
-            int pending = 0;
-            if (lane == 0)
-                pending = atomicAdd(p.ws, 1);
+            int pending = (int)blockIdx.x;
             for (int k = 0; ok; ++k) {
                 // item k: its claim number, then its work-list entry (lanes 0-1 load the two halves)
                 if (k >= kQueue &&
@@ -738,8 +742,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ========================= TMA producer: V =========================
             // Copies each item's V tiles into the V ring as soon as the PV issuer frees a slot,
             // independently of the K stream.
-            if (lane == 0)
-                prefetch_tmap(&tmap_v);
             bool ok = true;
             int j = 0;                                  // global key tile of the next V copy
             Item it;
@@ -1210,11 +1212,12 @@ int nvkv_host::tile_attention(const TileAttnArgs &a)
         if (attr_state[dev] != 1)
             return attr_state[dev];
     }
-    prefill_plan_kernel<<<1, kPlanThreads, 0, a.stream>>>(pp);
     // persistent: one CTA per SM (shared memory and TMEM admit one); CTAs claim the work list's
     // entries in order
     const int64_t claims = cap * num_kv_heads;
     const int grid = (int)(claims < sms ? claims : sms);
+    pp.grid = grid;
+    prefill_plan_kernel<<<1, kPlanThreads, 0, a.stream>>>(pp);
     // launched as a programmatic dependent of the pre-pass: its CTAs set up (barriers, TMEM, tensor
     // maps) while the pre-pass runs, and wait for the work list with griddepcontrol.wait
     cudaLaunchConfig_t cfg{};
