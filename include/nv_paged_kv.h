@@ -337,7 +337,8 @@ int nv_paged_decode_attn_noalloc(const void *q, const void *k_cache, const void 
  *                 16-byte aligned, else NV_ERR_WORKSPACE.  The call first writes into it (on
  *                 `stream`, a one-CTA pre-pass) the list of query tiles -- sequence by
  *                 sequence, heaviest sequence first, each sequence's tiles heaviest first -- and
- *                 the counter from which the persistent CTAs claim them, so it needs no
+ *                 how the persistent CTAs claim them (the first three quarters dealt round-robin,
+ *                 the rest from a counter), so it needs no
  *                 initialisation; calls that share a workspace must not overlap on the device.
  *                 A batch whose tiles would not fit (cu_seqlens_q inconsistent with total_q) sets
  *                 NV_DERR_LENGTH and leaves the last-listed tiles uncomputed.

@@ -13,8 +13,9 @@
 // the next tile's first scores are computed while the current tile finishes.
 //   * a one-CTA pre-pass lists the non-empty query tiles in the caller's workspace, sequence by
 //     sequence (heaviest sequence first, each sequence's tiles heaviest first), so the CTAs at
-//     work share a few sequences' K/V in L2; CTA i takes claim i first, and every later claim
-//     is one atomic add on a counter there.
+//     work share a few sequences' K/V in L2.  The first three quarters of the claims are dealt
+//     round-robin (CTA i takes i, i + grid, ...); the rest go to whichever CTA asks first, one
+//     atomic add on a counter there each.
 //   * warps 4 and 11 (TMA producers): warp 4 claims tiles and passes them to the other warps
 //     through a small queue in shared memory, and copies each tile's Q (one 3-D tensor-map copy
 //     per 64-dim half; dims head_dim, q head, token) into one of two Q buffers and its K tiles
@@ -198,9 +199,12 @@ struct Item {
 
 // ---------------------------------------------------------------------------------------
 // Work list.  A one-CTA pre-pass lists every non-empty query tile of every sequence (all kv
-// heads share an entry) in the workspace, validates the lengths, and starts the claim counter at
-// the main kernel's grid size: CTA i's first claim is i itself, so the first items of all CTAs are
-// not serialised on one atomic as the CTAs start together.
+// heads share an entry) in the workspace, validates the lengths, and sets up the claims: the first
+// m rounds of grid-size claims (m = 3/4 of all claims / grid, at least 1) are static, CTA i taking
+// i, i + grid, ..., i + (m-1) grid, and the counter starts at m * grid for the rest.  A claim from
+// the counter is an atomic whose answer the producer warp waits for at the item boundary (~1,400
+// cycles); the static rounds have none, and the dynamic last quarter still evens out the CTAs'
+// finishing times, as the list runs heaviest first.
 // The list runs sequence by sequence, heaviest sequence first (a counting sort on the key steps
 // of its last tile), and within a sequence from its last (heaviest) tile to its first.  So the
 // CTAs busy at any moment work on one or two sequences, whose K/V then stays in L2 while every
@@ -208,7 +212,7 @@ struct Item {
 // batch's K/V from HBM once per wave), and the lightest tiles still come last.  The main
 // kernel's claim number v then names entry v / Hkv and kv head v % Hkv: a claim is at most one
 // atomic add and one 32-byte record load, with no empty tiles to skip.
-//   workspace ints: [0] claim counter, [1] entries, [16 + 8e ...] entry e:
+//   workspace ints: [0] claim counter, [1] entries, [2] static rounds m, [16 + 8e ...] entry e:
 //   {b, cq0, Lq, P, i0, nq, kv_len, nkv}
 // ---------------------------------------------------------------------------------------
 constexpr int kPlanThreads = 1024;
@@ -226,7 +230,8 @@ struct PlanParams {
     int32_t max_len;         // decode mode: longer contexts are truncated to this (NV_DERR_LENGTH)
     int32_t row_u4;          // decode mode: 16-byte words per output row
     int32_t split_steps;     // decode mode: key steps per entry (0: one entry per sequence)
-    int32_t grid;            // CTAs of the main kernel: claims below it are taken by CTA index
+    int32_t grid;            // CTAs of the main kernel
+    int32_t num_kv_heads;    // claims per work-list entry
 };
 
 __device__ __forceinline__ bool plan_seq(const PlanParams &pp, int b, int &cq0, int &Lq, int &P, int &T)
@@ -371,8 +376,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) prefill_plan_kernel(const Pla
     if (tid == 0) {
         if (count > pp.cap)
             flag_error(pp.d_err, NV_DERR_LENGTH);
-        pp.ws[0] = pp.grid;
-        pp.ws[1] = min(count, pp.cap);
+        const int entries = min(count, pp.cap);
+        const long long claims = (long long)entries * pp.num_kv_heads;
+        const int m = max(1, (int)(claims * 3 / 4 / pp.grid));
+        pp.ws[0] = pp.grid * m;
+        pp.ws[1] = entries;
+        pp.ws[2] = m;
     }
 }
 
@@ -652,11 +661,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // its K tiles into the K ring as the S issuer frees the slots.
             bool ok = true;
             int j = 0;                                  // global key tile of the next K copy
-            // lane 0 claims one item ahead: the counter's answer for item k+1 travels while item k's
-            // copies are issued.  The first claim is the CTA's index (the counter starts at the grid
-            // size).
+            // Item k+1's claim is known as item k starts: CTA index + (k+1) * grid for the first
+            // m_static items, else the counter's answer, which lane 0 asks for then and which travels
+            // while item k's copies are issued.
             const int4 *plan = reinterpret_cast<const int4 *>(p.ws + kPlanHeaderInts);
             int pending = (int)blockIdx.x;
+            const int m_static = p.ws[2];
             for (int k = 0; ok; ++k) {
                 // item k: its claim number, then its work-list entry (lanes 0-1 load the two halves)
                 if (k >= kQueue &&
@@ -665,7 +675,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const int v = __shfl_sync(0xffffffffu, pending, 0);
-                if (lane == 0 && v < total)
+                if (k + 1 < m_static)
+                    pending = v + (int)gridDim.x;
+                else if (lane == 0 && v < total)
                     pending = atomicAdd(p.ws, 1);
                 Item it{};
                 it.v = v < total ? v : total;
@@ -1217,6 +1229,7 @@ int nvkv_host::tile_attention(const TileAttnArgs &a)
     const int64_t claims = cap * num_kv_heads;
     const int grid = (int)(claims < sms ? claims : sms);
     pp.grid = grid;
+    pp.num_kv_heads = num_kv_heads;
     prefill_plan_kernel<<<1, kPlanThreads, 0, a.stream>>>(pp);
     // launched as a programmatic dependent of the pre-pass: its CTAs set up (barriers, TMEM, tensor
     // maps) while the pre-pass runs, and wait for the work list with griddepcontrol.wait
