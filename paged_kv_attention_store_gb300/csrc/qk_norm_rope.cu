@@ -17,7 +17,9 @@
 // use them with shuffles.  Values are held as fp32 pairs and the arithmetic uses the packed pair
 // instructions (squares, the scaling by 1/rms and the rotation); the two bf16 roundings also work
 // on pairs (one conversion rounds two normalised values, one bf16x2 multiply forms both weight
-// products).  The loads of kBatch groups of four heads go out together before any arithmetic.
+// products).  All of a token's heads (kBatch groups of four) are loaded before any arithmetic, and
+// the next token's position and slot one token ahead, so each token costs one memory latency rather
+// than three; a padding token's k and v rows are read although nothing of them is stored.
 // The RoPE frequencies are computed once per call on the host (64 floats, passed as a kernel
 // parameter); the angle product and sincosf are fp32, as the pages compute them.
 #include <cmath>
@@ -30,9 +32,9 @@ using namespace nvkv;
 
 constexpr int kD = 128;
 constexpr int kGroup = 4;              // heads per warp instruction (8 lanes each)
-constexpr int kBatch = 4;              // groups of four heads whose loads go out together
+constexpr int kBatch = 8;              // groups of four heads whose loads go out together
 constexpr int kWarps = 4;              // per block
-constexpr int kBlocksPerSm = 4;        // 116 registers a thread: four 128-thread blocks per SM
+constexpr int kBlocksPerSm = 3;        // 158 registers a thread: three 128-thread blocks per SM
 
 struct RopeParams {
     const __nv_bfloat16 *qkv;
@@ -109,9 +111,16 @@ __global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm)
     // lane l computes the angles of frequencies 2l and 2l+1
     const float f0 = p.inv_freq[2 * lane], f1 = p.inv_freq[2 * lane + 1];
 
+    int nxt_pos = warp_id < p.n_tokens ? __ldg(p.positions + warp_id) : 0;      // one token ahead
+    int nxt_slot = warp_id < p.n_tokens ? __ldg(p.slot_mapping + warp_id) : -1;
     for (int64_t t = warp_id; t < p.n_tokens; t += nwarps) {
         const uint4 *row = reinterpret_cast<const uint4 *>(p.qkv + t * p.row_stride);
-        const float pos = (float)__ldg(p.positions + t);
+        const float pos = (float)nxt_pos;
+        const int sraw = nxt_slot;
+        if (t + nwarps < p.n_tokens) {
+            nxt_pos = __ldg(p.positions + t + nwarps);
+            nxt_slot = __ldg(p.slot_mapping + t + nwarps);
+        }
         float s0, c0, s1, c1;
         sincosf(pos * f0, &s0, &c0);
         sincosf(pos * f1, &s1, &c1);
@@ -125,7 +134,6 @@ __global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm)
             sn[m] = make_float2(__shfl_sync(0xffffffffu, s0, src), __shfl_sync(0xffffffffu, s1, src));
             nsn[m] = make_float2(-sn[m].x, -sn[m].y);
         }
-        const int sraw = __ldg(p.slot_mapping + t);
         const bool store = sraw >= 0 && sraw < p.num_slots;
         if (lane == 0 && (sraw < -1 || sraw >= p.num_slots))
             flag_error(p.d_err, NV_DERR_SLOT_RANGE);
@@ -136,7 +144,7 @@ __global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm)
             for (int i = 0; i < kBatch; ++i) {
                 const int h = h0 + kGroup * i + gi;
                 a[i] = b[i] = make_uint4(0, 0, 0, 0);
-                if (h < heads && (h < p.num_q_heads || store)) {
+                if (h < heads) {
                     a[i] = __ldg(row + h * (kD / 8) + li);          // dims 8li .. 8li+7
                     b[i] = __ldg(row + h * (kD / 8) + 8 + li);      // dims 64+8li .. 64+8li+7
                 }
