@@ -8,9 +8,10 @@
 // How (GB300 design; the pages call a library kernel here).  The unit of work is one 128-row
 // query tile of one (sequence, kv head); with G = Hq/Hkv query heads per kv head the tile packs
 // 128/G consecutive tokens x G heads, so every K/V tile loaded serves all G heads.  The kernel
-// is persistent (one CTA per SM): CTAs claim tiles in work-list order from a counter in the
-// caller's workspace, and each CTA runs its tiles as one continuous stream of 128-key steps, so
-// the next tile's first scores are computed while the current tile finishes.
+// is persistent (one CTA per SM): CTAs take tiles in work-list order (dealt round-robin, then
+// claimed from a counter in the caller's workspace), and each CTA runs its tiles as one continuous
+// stream of 128-key steps, so the next tile's first scores are computed while the current tile
+// finishes.
 //   * a one-CTA pre-pass lists the non-empty query tiles in the caller's workspace, sequence by
 //     sequence (heaviest sequence first, each sequence's tiles heaviest first), so the CTAs at
 //     work share a few sequences' K/V in L2.  The first three quarters of the claims are dealt
@@ -32,12 +33,14 @@
 //     latency in the issuing thread (barrier waits, commits, bookkeeping) idles the tensor pipe;
 //     with two issuers one warp's waits overlap the other's MMAs (a single alternating issuer
 //     measured 25% slower).  Operand descriptors are precomputed per buffer.
-//   * warps 0-3 (softmax / correction / epilogue): thread r owns row r = TMEM lane r.  It loads
-//     its 128 scores at once, masks only on steps that cross the diagonal (a separate code
-//     path), keeps a base-2 online softmax with a lazy rescale (the running max moves only when
-//     a score beats it by more than 8; only then is O rescaled in TMEM), and writes P with
-//     tcgen05.st.  At a tile's end it normalises O, stages the bf16 rows in the tile's Q buffer
-//     (free once the last PV is done) and writes them with tensor-map stores.
+//   * warps 0-3 (softmax / correction): thread r owns row r = TMEM lane r.  It loads its 128
+//     scores at once, masks only on steps that cross the diagonal (a separate code path), keeps
+//     a base-2 online softmax with a lazy rescale (the running max moves only when a score beats
+//     it by more than 8; only then is O rescaled in TMEM), and writes P with tcgen05.st.  At a
+//     tile's end it hands the row sums to warps 7-10 and goes on with the next tile.
+//   * warps 7-10 (epilogue; TMEM lane quarter = warp % 4): read O, normalise it, stage the bf16
+//     rows in the tile's Q buffer (free once the last S has read it) and write them with
+//     tensor-map stores.
 // Measured on GB300: an M=128 K=16 tcgen05.mma fed back to back takes 64 cycles at N=128 and 48
 // at N=64 (so key steps are 128 wide), and loading 128 fp32 scores from TMEM takes ~30 cycles.
 // Every mbarrier wait is bounded; on timeout the kernel records NV_DERR_TIMEOUT and stops.
