@@ -211,8 +211,9 @@ size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
  * block_size + j % block_size.  fp32 accumulation and softmax, bf16 output rounded once.
  * A row with L == 0 (graph padding) gets zeros.
  *
- * Groups (num_q_heads / num_kv_heads) 1 and 2, and group 4 for batches of at most 16 sequences or
- * whose split-KV grid spans at least ten waves of the GPU (the 512-sequence Qwen3-8B batch): a
+ * Groups (num_q_heads / num_kv_heads) 1 and 2, and group 4 for batches of at most 16 sequences
+ * with num_seqs x max_context_len below 32768 or whose split-KV grid spans at least ten waves of
+ * the GPU (the 512-sequence Qwen3-8B batch): a
  * split-KV flash-decoding kernel on CUDA cores (one launch; a second one merges the partials when a
  * sequence spans more than 16 splits).  Groups 8 and 16, and group 4 in between: the tcgen05 tile
  * kernel of nv_paged_prefill_attn with one query row per sequence at position L-1 (two launches: a
@@ -220,7 +221,8 @@ size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
  * fewer than two (sequence, kv head) units per SM has its keys split into ranges of at least 1024,
  * and a third launch merges them).  At group 8 the CUDA-core kernel's FMAs no longer keep up with
  * HBM (measured 0.54 of the roofline); at group 4 the tile kernel's persistent schedule fills the
- * GPU where a short split-KV grid cannot (64 sequences: 109 against 150 us), and it keeps up when
+ * GPU where a short split-KV grid cannot (64 sequences: 109 against 150 us; one 128K-token
+ * sequence: 97 against 170 us), and it keeps up when
  * shared prefix blocks come from L2 and the CUDA-core consumers are bound by their FMAs.  The two
  * paths round differently (P is rounded to bf16 before the PV product on the tile kernel); both
  * are within the parity bar of the fp32 definition.

@@ -687,12 +687,20 @@ constexpr int kTileGroup = 8;
 // headline-sized batch (512 sequences, 13 waves) is HBM-bound on CUDA cores at 0.98 of the copy
 // peak and stays there; at 16 sequences or fewer the split-KV kernel is the faster one (51 against
 // 56 us at 8).  G = 1, 2 always use the split-KV kernel (G = 2, 256 sequences: 180 against 189 us).
+// Group 4, 16 sequences or fewer: the tile kernel once num_seqs x max_context_len reaches 32768 keys
+// (one 32K-token sequence 50 against 64 us on the split-KV kernel, one of 128K 97 against 170 us,
+// four of 32K 96 against 119 us); below that the batch is a few tens of MB, latency-bound on either
+// kernel, and the split-KV launch is 2-4 us quicker.
+constexpr int64_t kTileMinKeysSmallBatch = 32768;
+
 bool decode_on_tiles_rule(int group, int num_seqs, int max_context_len)
 {
     if (group >= kTileGroup)
         return true;
-    if (group != 4 || num_seqs <= 16)
+    if (group != 4)
         return false;
+    if (num_seqs <= 16)
+        return (int64_t)num_seqs * max_context_len >= kTileMinKeysSmallBatch;
     const int split = decode_split_tokens(num_seqs, max_context_len);
     const int64_t units = (int64_t)num_seqs * ((max_context_len + split - 1) / split);
     const int sms = nvkv_host::sm_count();

@@ -109,6 +109,14 @@ def test_decode_group4_mid_batches_on_tiles(num_seqs):
     _full(W.qwen8_decode(num_seqs=num_seqs), f"group4 {num_seqs} seqs")
 
 
+@pytest.mark.parametrize("lens,bs,pad", [([40000], 256, 0), ([20000, 13000, 7], 256, 0), ([33000, 2], 16, 1)],
+                         ids=["one-40k", "three-mixed", "bs16-with-padding-row"])
+def test_decode_group4_few_long_contexts_on_tiles(lens, bs, pad):
+    """Group 4 with a few long contexts (num_seqs x max_context_len >= 32768 keys) decodes on the tile
+    kernel with its keys split into ranges: every sequence against the oracle (a padding row gets zeros)."""
+    _full(W.make_decode("g4-few-long", 31, lens, 32, 8, 128, bs, n_pad=pad), f"group4 few long {lens}")
+
+
 def test_decode_block_permutation_invariance():
     b = W.make_decode("perm", 23, [40, 700, 1200], 16, 8, 128, 64)
     db, got, kc, vc = _run(b)

@@ -54,6 +54,8 @@ CASES = [
     # group 4 with 17-40 sequences decodes on the tile kernel: store pass + tile decode
     ("g4-tiles-24", list(np.random.default_rng(5).integers(1, 3000, 24)), 32, 8, 128, 2),
     ("g4-tiles-40-bs16", list(np.random.default_rng(6).integers(1, 2000, 40)), 32, 8, 16, 0),
+    # group 4, a few long contexts (>= 32768 keys in all): also the tile kernel, keys split
+    ("g4-few-long", [40000, 7, 1300], 32, 8, 256, 1),
 ]
 
 
