@@ -677,7 +677,7 @@ constexpr int kTileGroup = 8;
 
 // Which kernel decodes a batch.  G >= 8: the tile kernel (above).  G = 4: the split-KV kernel for
 // batches whose grid spans at least ten waves of the GPU (two CTAs per SM), and for batches of at
-// most 16 sequences; the tile kernel in between.  Measured at G = 4 (32 q / 8 kv heads, contexts
+// most 16 sequences with short contexts; the tile kernel otherwise.  Measured at G = 4 (32 q / 8 kv heads, contexts
 // U[1024, 4096]): the split-KV grid of a mid-sized batch ends in a partly filled last wave and
 // pays each CTA's start (barriers, a pipeline refilled from HBM) per (sequence, split): 64
 // sequences 149.5 us (4.3 TB/s) against 109.2 us (5.9 TB/s) on the tile kernel, whose persistent
@@ -685,9 +685,9 @@ constexpr int kTileGroup = 8;
 // 392 us; and when most of the KV is shared and sits in L2 (64 sequences sharing 3072 of their
 // 4096 positions) the split-KV consumers are bound by their own FMAs: 172 against 123 us.  The
 // headline-sized batch (512 sequences, 13 waves) is HBM-bound on CUDA cores at 0.98 of the copy
-// peak and stays there; at 16 sequences or fewer the split-KV kernel is the faster one (51 against
-// 56 us at 8).  G = 1, 2 always use the split-KV kernel (G = 2, 256 sequences: 180 against 189 us).
-// Group 4, 16 sequences or fewer: the tile kernel once num_seqs x max_context_len reaches 32768 keys
+// peak and stays there.  G = 1, 2 always use the split-KV kernel (G = 2, 256 sequences: 180 against
+// 189 us).  Group 4, 16 sequences or fewer: the split-KV kernel is the faster one on short contexts
+// (51 against 56 us at 8 of U[1024, 4096]), the tile kernel once num_seqs x max_context_len reaches 32768 keys
 // (one 32K-token sequence 50 against 64 us on the split-KV kernel, one of 128K 97 against 170 us,
 // four of 32K 96 against 119 us); below that the batch is a few tens of MB, latency-bound on either
 // kernel, and the split-KV launch is 2-4 us quicker.
