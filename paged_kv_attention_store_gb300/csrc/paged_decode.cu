@@ -675,7 +675,8 @@ int run_split_kv(int group, DecodeParams &p, int num_seqs, cudaStream_t st)
 // about 1.0 for the tile kernel on the same batch).  Its work list sits after the split counters.
 constexpr int kTileGroup = 8;
 
-// Which kernel decodes a batch.  G >= 8: the tile kernel (above).  G = 4: the split-KV kernel for
+// Which kernel decodes a batch.  G >= 8: the tile kernel (above).  G = 1, 2: the split-KV kernel
+// except for a few long contexts (below).  G = 4: the split-KV kernel for
 // batches whose grid spans at least ten waves of the GPU (two CTAs per SM), and for batches of at
 // most 16 sequences with short contexts; the tile kernel otherwise.  Measured at G = 4 (32 q / 8 kv heads, contexts
 // U[1024, 4096]): the split-KV grid of a mid-sized batch ends in a partly filled last wave and
@@ -690,15 +691,18 @@ constexpr int kTileGroup = 8;
 // (51 against 56 us at 8 of U[1024, 4096]), the tile kernel once num_seqs x max_context_len reaches 32768 keys
 // (one 32K-token sequence 50 against 64 us on the split-KV kernel, one of 128K 97 against 170 us,
 // four of 32K 96 against 119 us); below that the batch is a few tens of MB, latency-bound on either
-// kernel, and the split-KV launch is 2-4 us quicker.
+// kernel, and the split-KV launch is 2-4 us quicker.  Groups 1 and 2, whose CUDA-core consumers have
+// less arithmetic per byte: the tile kernel only for at most 4 sequences with contexts of 32768 or
+// more (group 2: one of 128K 97 against 164 us, two of 64K 99 against 129 us, four of 32K 95 against
+// 111 us; but six of 32K 140 against 137 us and twelve of 16K 140 against 133 us).
 constexpr int64_t kTileMinKeysSmallBatch = 32768;
 
 bool decode_on_tiles_rule(int group, int num_seqs, int max_context_len)
 {
     if (group >= kTileGroup)
         return true;
-    if (group != 4)
-        return false;
+    if (group < 4)
+        return num_seqs <= 4 && max_context_len >= kTileMinKeysSmallBatch;
     if (num_seqs <= 16)
         return (int64_t)num_seqs * max_context_len >= kTileMinKeysSmallBatch;
     const int split = decode_split_tokens(num_seqs, max_context_len);

@@ -117,6 +117,15 @@ def test_decode_group4_few_long_contexts_on_tiles(lens, bs, pad):
     _full(W.make_decode("g4-few-long", 31, lens, 32, 8, 128, bs, n_pad=pad), f"group4 few long {lens}")
 
 
+@pytest.mark.parametrize("hq,hkv,lens", [(8, 8, [40000]), (16, 8, [33000, 5]), (16, 8, [36000, 70, 33000, 1]),
+                                         (16, 8, [33000] * 5)],
+                         ids=["g1-one-40k", "g2-two", "g2-four", "g2-five-split-kv"])
+def test_decode_groups_1_2_few_long_contexts(hq, hkv, lens):
+    """Groups 1 and 2 with at most 4 sequences and a context of 32768 or more decode on the tile kernel;
+    five such sequences stay on the split-KV kernel: every sequence against the oracle."""
+    _full(W.make_decode("g12-few-long", 37, lens, hq, hkv, 128, 256), f"group {hq // hkv} few long {len(lens)}")
+
+
 def test_decode_block_permutation_invariance():
     b = W.make_decode("perm", 23, [40, 700, 1200], 16, 8, 128, 64)
     db, got, kc, vc = _run(b)

@@ -56,6 +56,7 @@ CASES = [
     ("g4-tiles-40-bs16", list(np.random.default_rng(6).integers(1, 2000, 40)), 32, 8, 16, 0),
     # group 4, a few long contexts (>= 32768 keys in all): also the tile kernel, keys split
     ("g4-few-long", [40000, 7, 1300], 32, 8, 256, 1),
+    ("g2-few-long", [35000, 3], 16, 8, 256, 0),
 ]
 
 
