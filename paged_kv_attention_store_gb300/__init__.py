@@ -99,18 +99,19 @@ def _check(fn, rc):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()      # ctypes passes an int as the c_void_p argument
 
 
 def _stream(stream):
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    return s.cuda_stream                            # an int, passed as the c_void_p argument
 
 
 def _need(cond, msg):
+    """Raise ValueError(msg) unless ``cond``; ``msg`` may be a callable, formatted only on failure."""
     if not cond:
-        raise ValueError(msg)
+        raise ValueError(msg() if callable(msg) else msg)
 
 
 def _dtypes(bf16=(), i32=(), f32=()):
@@ -118,21 +119,22 @@ def _dtypes(bf16=(), i32=(), f32=()):
     import torch
     for want, group in ((torch.bfloat16, bf16), (torch.int32, i32), (torch.float32, f32)):
         for name, t in group:
-            if t is not None:
-                _need(t.dtype == want, f"{name} must be {str(want).replace('torch.', '')}, not {t.dtype}")
+            if t is not None and t.dtype != want:
+                raise ValueError(f"{name} must be {str(want).replace('torch.', '')}, not {t.dtype}")
 
 
 def _on_one_gpu(*named):
     """Every tensor given (None = absent) lives on the same CUDA device; returns that device."""
-    dev = None
+    first = None
     for name, t in named:
         if t is None:
             continue
-        _need(t.is_cuda, f"{name} must be a CUDA tensor (it is on {t.device})")
-        if dev is None:
-            dev = t.device
-        _need(t.device == dev, f"{name} is on {t.device}, the other tensors on {dev}")
-    return dev
+        _need(t.is_cuda, lambda: f"{name} must be a CUDA tensor (it is on {t.device})")
+        if first is None:
+            first, idx = t, t.get_device()
+        elif t.get_device() != idx:
+            raise ValueError(f"{name} is on {t.device}, the other tensors on {first.device}")
+    return None if first is None else first.device
 
 
 # Default workspaces: one per (device, stream, kind), grown when a call needs more and kept, so a
@@ -176,8 +178,8 @@ def nv_store_kvcache(k, v, slot_mapping, k_cache, v_cache, d_err=None, stream=No
     _need(slot_mapping.dim() == 1 and slot_mapping.is_contiguous(), "slot_mapping must be a contiguous [N]")
     n = int(slot_mapping.shape[0])
     for name, t in (("k", k), ("v", v)):
-        _need(t.dim() == 3 and tuple(t.shape) == (n, hkv, d), f"{name} must be [N, Hkv, D] = {(n, hkv, d)}")
-        _need(t.stride(2) == 1 and t.stride(1) == d, f"{name} heads must be contiguous")
+        _need(t.dim() == 3 and tuple(t.shape) == (n, hkv, d), lambda: f"{name} must be [N, Hkv, D] = {(n, hkv, d)}")
+        _need(t.stride(2) == 1 and t.stride(1) == d, lambda: f"{name} heads must be contiguous")
     _dtypes(bf16=(("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache)),
             i32=(("slot_mapping", slot_mapping), ("d_err", d_err)))
     _on_one_gpu(("k", k), ("v", v), ("slot_mapping", slot_mapping), ("k_cache", k_cache), ("v_cache", v_cache),
@@ -200,7 +202,7 @@ def _ws_arg(workspace, name):
     import torch
     if workspace is None:
         return None, 0
-    _need(workspace.dtype == torch.uint8 and workspace.is_contiguous(), f"{name} must be a contiguous uint8 tensor")
+    _need(workspace.dtype == torch.uint8 and workspace.is_contiguous(), lambda: f"{name} must be a contiguous uint8 tensor")
     return _ptr(workspace), workspace.numel()
 
 
@@ -209,9 +211,9 @@ def _check_out(out, shape, name="out"):
     import torch
     if out is None:
         return
-    _need(tuple(out.shape) == tuple(shape), f"{name} must be {tuple(shape)}, not {tuple(out.shape)}")
-    _need(out.dtype == torch.bfloat16, f"{name} must be bfloat16, not {out.dtype}")
-    _need(out.is_contiguous(), f"{name} must be contiguous")
+    _need(tuple(out.shape) == tuple(shape), lambda: f"{name} must be {tuple(shape)}, not {tuple(out.shape)}")
+    _need(out.dtype == torch.bfloat16, lambda: f"{name} must be bfloat16, not {out.dtype}")
+    _need(out.is_contiguous(), lambda: f"{name} must be contiguous")
 
 
 def _out_like(out, ref, shape):
@@ -220,8 +222,8 @@ def _out_like(out, ref, shape):
 
 
 def _vec(t, name, n=None):
-    _need(t.dim() == 1 and t.is_contiguous(), f"{name} must be a contiguous 1-D tensor")
-    _need(n is None or int(t.shape[0]) == n, f"{name} must have {n} entries, not {int(t.shape[0])}")
+    _need(t.dim() == 1 and t.is_contiguous(), lambda: f"{name} must be a contiguous 1-D tensor")
+    _need(n is None or int(t.shape[0]) == n, lambda: f"{name} must have {n} entries, not {int(t.shape[0])}")
 
 
 def _table(bt, rows):
@@ -404,8 +406,8 @@ def nv_store_decode_attn(q, k, v, slot_mapping, k_cache, v_cache, block_tables, 
           "slot_mapping must have one entry per sequence")
     _vec(slot_mapping, "slot_mapping", B)
     for name, t in (("k", k), ("v", v)):
-        _need(t.dim() == 3 and tuple(t.shape) == (B, hkv, d), f"{name} must be [B, Hkv, D] = {(B, hkv, d)}")
-        _need(t.stride(2) == 1 and t.stride(1) == d, f"{name} heads must be contiguous")
+        _need(t.dim() == 3 and tuple(t.shape) == (B, hkv, d), lambda: f"{name} must be [B, Hkv, D] = {(B, hkv, d)}")
+        _need(t.stride(2) == 1 and t.stride(1) == d, lambda: f"{name} heads must be contiguous")
     (nb, bs, hkv, d), B, hq, out = _decode_args(q, k_cache, v_cache, block_tables, context_lens, out, d_err,
                                                  workspace, (("k", k), ("v", v), ("slot_mapping", slot_mapping)))
     if max_context_len is None:
