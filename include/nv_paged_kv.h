@@ -211,10 +211,10 @@ size_t nv_paged_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int
  * block_size + j % block_size.  fp32 accumulation and softmax, bf16 output rounded once.
  * A row with L == 0 (graph padding) gets zeros.
  *
- * Groups (num_q_heads / num_kv_heads) 1 and 2 (except at most 4 sequences with max_context_len of
- * 32768 or more), and group 4 for batches of at most 16 sequences with num_seqs x max_context_len
- * below 32768 or whose split-KV grid spans at least ten waves of the GPU (the 512-sequence
- * Qwen3-8B batch): a
+ * Groups (num_q_heads / num_kv_heads) 1 and 2 (except at most 8 sequences with num_seqs x
+ * max_context_len of 32768 or more), and group 4 for batches of at most 16 sequences with
+ * num_seqs x max_context_len below 32768 or whose split-KV grid spans at least ten waves of the
+ * GPU (the 512-sequence Qwen3-8B batch): a
  * split-KV flash-decoding kernel on CUDA cores (one launch; a second one merges the partials when a
  * sequence spans more than 16 splits).  Groups 8 and 16, and the other batches: the tcgen05 tile
  * kernel of nv_paged_prefill_attn with one query row per sequence at position L-1 (two launches: a

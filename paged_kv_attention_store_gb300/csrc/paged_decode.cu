@@ -692,9 +692,10 @@ constexpr int kTileGroup = 8;
 // (one 32K-token sequence 50 against 64 us on the split-KV kernel, one of 128K 97 against 170 us,
 // four of 32K 96 against 119 us); below that the batch is a few tens of MB, latency-bound on either
 // kernel, and the split-KV launch is 2-4 us quicker.  Groups 1 and 2, whose CUDA-core consumers have
-// less arithmetic per byte: the tile kernel only for at most 4 sequences with contexts of 32768 or
-// more (group 2: one of 128K 97 against 164 us, two of 64K 99 against 129 us, four of 32K 95 against
-// 111 us; but six of 32K 140 against 137 us and twelve of 16K 140 against 133 us).
+// less arithmetic per byte: the tile kernel for at most 8 sequences holding 32768 keys or more (GPU
+// time in a CUDA graph at group 2, split-KV against tiles: two of 16K 41.2 / 33.2 us, four of 8K
+// 36.5 / 32.4, eight of 8K 60.1 / 53.1, eight of 16K 97.0 / 90.8, one of 32K 54.6 / 35.5, one of 128K
+// 164 / 97); from 12 sequences the split-KV kernel is as fast or faster (twelve of 16K 125.9 / 134.8).
 constexpr int64_t kTileMinKeysSmallBatch = 32768;
 
 bool decode_on_tiles_rule(int group, int num_seqs, int max_context_len)
@@ -702,7 +703,7 @@ bool decode_on_tiles_rule(int group, int num_seqs, int max_context_len)
     if (group >= kTileGroup)
         return true;
     if (group < 4)
-        return num_seqs <= 4 && max_context_len >= kTileMinKeysSmallBatch;
+        return num_seqs <= 8 && (int64_t)num_seqs * max_context_len >= kTileMinKeysSmallBatch;
     if (num_seqs <= 16)
         return (int64_t)num_seqs * max_context_len >= kTileMinKeysSmallBatch;
     const int split = decode_split_tokens(num_seqs, max_context_len);

@@ -117,12 +117,13 @@ def test_decode_group4_few_long_contexts_on_tiles(lens, bs, pad):
     _full(W.make_decode("g4-few-long", 31, lens, 32, 8, 128, bs, n_pad=pad), f"group4 few long {lens}")
 
 
-@pytest.mark.parametrize("hq,hkv,lens", [(8, 8, [40000]), (16, 8, [33000, 5]), (16, 8, [36000, 70, 33000, 1]),
-                                         (16, 8, [33000] * 5)],
-                         ids=["g1-one-40k", "g2-two", "g2-four", "g2-five-split-kv"])
+@pytest.mark.parametrize("hq,hkv,lens", [(8, 8, [40000]), (16, 8, [33000, 5]), (16, 8, [9000] * 8),
+                                         (16, 8, [5000] * 9)],
+                         ids=["g1-one-40k", "g2-two", "g2-eight-tiles", "g2-nine-split-kv"])
 def test_decode_groups_1_2_few_long_contexts(hq, hkv, lens):
-    """Groups 1 and 2 with at most 4 sequences and a context of 32768 or more decode on the tile kernel;
-    five such sequences stay on the split-KV kernel: every sequence against the oracle."""
+    """Groups 1 and 2 with at most 8 sequences holding 32768 keys or more (num_seqs x max_context_len)
+    decode on the tile kernel; nine sequences stay on the split-KV kernel: every sequence against the
+    oracle."""
     _full(W.make_decode("g12-few-long", 37, lens, hq, hkv, 128, 256), f"group {hq // hkv} few long {len(lens)}")
 
 
