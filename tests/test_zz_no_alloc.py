@@ -51,8 +51,18 @@ def _group4_mid():
     return W.qwen8_decode(num_seqs=64)
 
 
-@pytest.mark.parametrize("make", [W.qwen06_decode, W.qwen8_decode, _group8, _group16, _group4_mid],
-                         ids=["qwen3-0.6b", "qwen3-8b", "group8-tiles", "group16-tiles", "group4-64seq-tiles"])
+def _group2_few_long():
+    return W.make_decode("group2-few-long", 8, [40000, 300], 16, 8, 128, 256, n_pad=1)
+
+
+def _group4_one_long():
+    return W.make_decode("group4-one-long", 9, [70000], 32, 8, 128, 256)
+
+
+@pytest.mark.parametrize("make", [W.qwen06_decode, W.qwen8_decode, _group8, _group16, _group4_mid, _group2_few_long,
+                                  _group4_one_long],
+                         ids=["qwen3-0.6b", "qwen3-8b", "group8-tiles", "group16-tiles", "group4-64seq-tiles",
+                              "group2-few-long-tiles", "group4-one-long-tiles"])
 def test_noalloc_matches_allocating_entry_point_twice(make):
     import torch
     b = make()
