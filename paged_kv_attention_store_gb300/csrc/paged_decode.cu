@@ -16,7 +16,9 @@
 //     is read from shared memory once and used G times (GQA sharing).  This kernel takes
 //     G = 1, 2, 4; with G = 8 or 16 the warps would do too many FMAs per KV byte to keep up
 //     with HBM, and decode runs on the tcgen05 tile kernel instead (tile_attention.cuh), as a
-//     prefill of one query row per sequence.  A half-warp handles
+//     prefill of one query row per sequence; so do mid-sized group-4 batches and a few long
+//     contexts at groups 1-4, where a split-KV grid fills the GPU poorly (decode_on_tiles_rule,
+//     below, with the measurements behind it).  A half-warp handles
 //     one position at a time, each lane 8 of the 128 dims; partial dot products are reduced
 //     with a reduce-scatter over 4 shuffle levels that leaves each lane the full score of
 //     one of the G heads, so the exponential is computed once per (position, head).
