@@ -127,6 +127,21 @@ def test_decode_groups_1_2_few_long_contexts(hq, hkv, lens):
     _full(W.make_decode("g12-few-long", 37, lens, hq, hkv, 128, 256), f"group {hq // hkv} few long {len(lens)}")
 
 
+def test_decode_group8_at_the_sequence_limit():
+    """65535 sequences of 1-16 positions at group 8 (8 q / 1 kv head, block size 16): the most the tile
+    kernel's work list addresses (one more is refused on the host).  Every sequence against the oracle."""
+    rng = np.random.default_rng(41)
+    b = W.make_decode("max-seqs", 41, rng.integers(1, 17, size=65535), 8, 1, 128, 16)
+    shape = (b.num_blocks, b.block_size, b.num_kv_heads, b.head_dim)
+    kc, vc = W.normal_bf16(rng, shape), W.normal_bf16(rng, shape)     # one draw each: quick to build
+    db = DeviceBatch(b, kc, vc)
+    db.store()
+    got = host_f32(db.decode())
+    assert db.err() == 0
+    kc1, vc1 = oracle_store_in_place(oracle.default(), b, kc, vc)
+    compare(got, oracle_decode(oracle.default(), b, kc1, vc1, threads=ORACLE_THREADS), "65535 sequences")
+
+
 def test_decode_block_permutation_invariance():
     b = W.make_decode("perm", 23, [40, 700, 1200], 16, 8, 128, 64)
     db, got, kc, vc = _run(b)

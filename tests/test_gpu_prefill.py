@@ -119,3 +119,22 @@ def test_prefill_many_sequences_and_long_chunk_sampled():
     rows = np.array(sorted(rows), np.int64)
     want = oracle_prefill(oracle.default(), b, kc, vc, rows=rows, threads=ORACLE_THREADS)
     compare(got[rows], want, "prefill many sequences")
+
+
+def test_prefill_at_the_sequence_limit():
+    """65535 sequences (the most the work list addresses; one more is refused on the host), chunks of
+    1-3 tokens over prefixes of 0-32, group 8 (8 q / 1 kv head), block size 16: every row against the
+    oracle."""
+    rng = np.random.default_rng(43)
+    n = 65535
+    b = W.make_prefill("max-seqs", 43, (rng.integers(0, 3, n) * 16).tolist(), rng.integers(1, 4, n).tolist(),
+                       8, 1, 128, 16)
+    shape = (b.num_blocks, b.block_size, b.num_kv_heads, b.head_dim)
+    kc0, vc0 = W.normal_bf16(rng, shape), W.normal_bf16(rng, shape)   # one draw each: quick to build
+    db = DeviceBatch(b, kc0, vc0)
+    db.store()
+    got = host_f32(db.prefill())
+    assert db.err() == 0
+    kc, vc = oracle_cache_after_store(oracle.default(), b, kc0, vc0)
+    compare(got, oracle_prefill(oracle.default(), b, kc, vc, threads=ORACLE_THREADS), "65535 sequences")
+
