@@ -1,4 +1,4 @@
-"""Seeded random shapes for decode and prefill against the oracle: group sizes 1-8 (kv heads 1-16), every supported
+"""Seeded random shapes for decode and prefill against the oracle: group sizes 1-16 (kv heads 1-16), every supported
 block size, lengths drawn around block and tile edges (1, bs-1, bs, bs+1, 127, 128, 129, ...), padding
 rows, and pools whose unused tails hold NaN patterns.  Small enough that the oracle runs every row."""
 import numpy as np
@@ -11,7 +11,7 @@ from tests.gpu_util import (ORACLE_THREADS, DeviceBatch, compare, host_f32, orac
 
 pytestmark = pytest.mark.gpu
 
-GROUPS = [(8, 8), (16, 8), (32, 8), (16, 2), (8, 1), (32, 16), (64, 8), (48, 12)]
+GROUPS = [(8, 8), (16, 8), (32, 8), (16, 2), (8, 1), (32, 16), (64, 8), (48, 12), (256, 16), (128, 16)]
 BLOCKS = [16, 32, 64, 128, 256]
 
 
@@ -27,7 +27,7 @@ def _edge_lengths(rng, bs, n, lo=1, hi=1500):
     return out
 
 
-@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("seed", range(10))
 def test_decode_random_shapes(seed):
     rng = np.random.default_rng([seed, 401])
     hq, hkv = GROUPS[seed % len(GROUPS)]
@@ -44,7 +44,7 @@ def test_decode_random_shapes(seed):
     assert not got[b.seq_lens == 0].any()
 
 
-@pytest.mark.parametrize("seed", range(8))
+@pytest.mark.parametrize("seed", range(10))
 def test_prefill_random_shapes(seed):
     rng = np.random.default_rng([seed, 402])
     hq, hkv = GROUPS[(seed + 3) % len(GROUPS)]
